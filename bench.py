@@ -1,0 +1,485 @@
+#!/usr/bin/env python3
+"""Benchmark: one step of the paged-KV attention hot path on GB300.
+
+A step is the whole path over one synthetic batch: the KV write of this
+step's new tokens (pa_write_kv) followed by attention for the batch
+(pa_attention: planner + split-KV kernel), with every input resident in HBM
+when timing starts. The headline workload is the Llama-3.1-8B-shaped decode
+batch (64 sequences, context U[512, 4096], 32 query / 8 KV heads, head_dim
+128, block_size 16); `value` is its algorithmic bytes per step divided by the
+device time per step (GB/s). The mixed chunked-prefill batch (512 decodes + 3
+chunks of 512, T = 2048) is measured in the same run and reported as
+tokens/s per layer under "mixed_batch".
+
+Timing: W warm-up steps, then K timed steps; before every step a buffer of
+twice the L2 size is written (outside the events) so no step starts with a
+warm L2; each step is bracketed by CUDA events on the launching stream. The
+decode kernel is also timed on its own (library timer events) for the
+roofline. SM clocks and throttle reasons are sampled with nvidia-smi while the
+timed loop runs.
+
+`--impl reference` times the CPU oracle (plain C, float64, all host cores) on
+a bounded sample of the same workload per step, and prints the same kind of
+line with "impl": "reference".
+
+With N > 1 (torchrun), every rank runs its own replica batch of the same
+shape (independent requests: weak scaling, no collective on the data path);
+timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_42_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-attn decode KV GB/s (frac of HBM peak); mixed-batch tokens/s per layer"
+HEADLINE_CONFIG = 2
+MIXED_CONFIG = 3
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one step (what a perfect implementation must move)
+# ---------------------------------------------------------------------------
+def step_bytes(w: wl.Workload) -> dict:
+    """Bytes one step must move at minimum (no re-reads, no partials)."""
+    D, Hq, Hkv, T = w.head_dim, w.num_q_heads, w.num_kv_heads, w.num_tokens
+    L = w.seq_lens.astype(np.int64)
+    nb = (L + 15) // 16
+    kv = int((L * Hkv * D * 2 * 2).sum())          # K and V rows, bf16
+    if w.shared_prefix_blocks:
+        # unique bytes: the shared prefix blocks are stored (and need reading) once
+        P = w.shared_prefix_blocks
+        kv_unique = kv - (w.num_reqs - 1) * P * 16 * Hkv * D * 2 * 2
+    else:
+        kv_unique = kv
+    qo = 2 * T * Hq * D * 2                         # q in, out out
+    meta = int(nb.sum()) * 4 + w.num_reqs * 8 + 4
+    attn = kv + qo + meta
+    write = 2 * T * Hkv * D * 2 * 2 + T * 8          # read k,v new; write cache rows
+    return {"kv": kv, "kv_unique": kv_unique, "attention": attn, "write": write,
+            "step": attn + write}
+
+
+def prefill_flops(w: wl.Workload) -> int:
+    f = 0
+    for r in range(w.num_reqs):
+        ql, ctx = int(w.q_lens[r]), int(w.ctx_lens[r])
+        if ql > 1:
+            f += sum(ctx + j + 1 for j in range(ql)) * w.num_q_heads * 4 * w.head_dim
+    return f
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return {"hbm_gbs": float(d["hbm_gbs"]), "source": "of measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "of fallback"}
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken with the decode kernel source as it is now; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    src = os.path.join(ROOT, "paged_kv_cache_42_gb300", "csrc", "decode.cu")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        e = d.get(workload)
+        if e and e.get("decode_cu_sha") == sha:
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; one process per GPU)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0, None
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return rank, ws, local, dist
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+class Resident:
+    """A workload resident on the device plus the pinned host copies used by
+    the end-to-end measurement."""
+
+    def __init__(self, w: wl.Workload, torch, binding):
+        self.w = w
+        self.torch = torch
+        self.binding = binding
+        dev = torch.device("cuda")
+
+        def bf(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+        self.h = {  # pinned host copies of the per-step inputs
+            "q": bf(w.q).pin_memory(), "k": bf(w.k_new).pin_memory(),
+            "v": bf(w.v_new).pin_memory(),
+            "slot_mapping": torch.from_numpy(w.slot_mapping).pin_memory(),
+            "block_tables": torch.from_numpy(w.block_tables).pin_memory(),
+            "seq_lens": torch.from_numpy(w.seq_lens).pin_memory(),
+            "qsl": torch.from_numpy(w.query_start_loc).pin_memory(),
+        }
+        self.d = {k: v.to(dev) for k, v in self.h.items()}
+        self.k_cache = bf(w.k_cache).to(dev)
+        self.v_cache = bf(w.v_cache).to(dev)
+        self.out = torch.empty_like(self.d["q"])
+        self.h_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        self.ws = torch.empty(binding.workspace_size(w.num_reqs, w.num_tokens, w.num_q_heads,
+                                                     w.num_kv_heads, w.head_dim),
+                              dtype=torch.uint8, device=dev)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.h.values())
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+
+    def step(self):
+        d, w, b = self.d, self.w, self.binding
+        b.write_kv(d["k"], d["v"], d["slot_mapping"], self.k_cache, self.v_cache)
+        b.attention(d["q"], self.k_cache, self.v_cache, d["block_tables"], d["seq_lens"],
+                    d["qsl"], w.scale, max_query_len=w.max_query_len,
+                    max_seq_len=w.max_seq_len, out=self.out, workspace=self.ws)
+
+    def step_e2e(self):
+        for k, t in self.h.items():
+            self.d[k].copy_(t, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, dist,
+               e2e: bool = False, clocks: ClockSampler | None = None):
+    fn = res.step_e2e if e2e else res.step
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    dk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in dk:  # materialise the event handles before handing them to the library
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    barrier(dist)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    n0 = binding.launch_count()
+    stream = torch.cuda.current_stream()
+    for i in range(steps):
+        flush()
+        binding.set_kernel_timer("decode", dk[i][0], dk[i][1])
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    binding.set_kernel_timer("decode", None, None)
+    launches = binding.launch_count() - n0
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    barrier(dist)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = [a.elapsed_time(b) for a, b in dk]
+    return {"ms_per_step": sum(step_ms) / steps, "ms_median": statistics.median(step_ms),
+            "decode_ms": sum(dec_ms) / steps, "launches": launches, "clocks": clk}
+
+
+def run_ours(args, rank, world, local, dist):
+    import torch
+
+    from paged_kv_cache_42_gb300 import binding
+    from paged_kv_cache_42_gb300 import build as libbuild
+
+    libbuild.build()
+    torch.cuda.set_device(local)
+    binding.init()
+    binding.get_device_error(clear=True)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.fill_(1)
+
+    peaks = measured_peaks()
+    result = {}
+    for idx in [args.config] + ([MIXED_CONFIG] if args.config != MIXED_CONFIG and not args.quick
+                                else []):
+        w = wl.make_config(idx, seed=42 + idx + 1000 * rank)
+        res = Resident(w, torch, binding)
+        sb = step_bytes(w)
+        steps = args.steps if idx == args.config else max(50, args.steps // 10)
+        t = time_steps(res, steps, args.warmup, flush, torch, binding, dist,
+                       clocks=ClockSampler(local) if idx == args.config else None)
+        code, detail = binding.get_device_error(clear=True)
+        if code:
+            raise RuntimeError(f"device error {code} at {detail}")
+        ms = max_over_ranks(t["ms_per_step"], dist)
+        dec_ms = max_over_ranks(t["decode_ms"], dist)
+        entry = {"w": w, "sb": sb, "t": t, "ms": ms, "dec_ms": dec_ms, "res": res,
+                 "steps": steps}
+        if idx == args.config and not args.no_e2e:
+            te = time_steps(res, max(20, steps // 4), args.warmup, flush, torch, binding, dist,
+                            e2e=True)
+            entry["e2e_ms"] = max_over_ranks(te["ms_per_step"], dist)
+        result[idx] = entry
+        if idx != args.config:
+            del res
+            entry["res"] = None
+            torch.cuda.empty_cache()
+
+    main = result[args.config]
+    w, sb = main["w"], main["sb"]
+    ms = main["ms"]
+    value = world * sb["step"] / (ms * 1e-3) / 1e9
+    achieved = sb["attention"] / (main["dec_ms"] * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": main["steps"],
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64, N(0,1) rounded to bf16)",
+        "config": {"workload": f"{wl.CONFIG_NAMES[args.config]}: "
+                               f"{wl.CONFIG_DESCRIPTIONS[args.config]}",
+                   "num_reqs": w.num_reqs, "num_tokens": w.num_tokens,
+                   "l2": "flushed before every timed step (2x L2 written)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {
+            "bound": "hbm", "kernel": "pa_decode_kernel",
+            "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+            "traffic": ncu_traffic(wl.CONFIG_NAMES[args.config]),
+            "algorithmic_bytes_per_launch": sb["attention"],
+            "kernel_ms": round(main["dec_ms"], 5)},
+        "gpu_launches": int(main["t"]["launches"]),
+        "clocks": main["t"]["clocks"],
+    }
+    if w.shared_prefix_blocks:
+        line["roofline"]["achieved_unique"] = round(
+            (sb["attention"] - sb["kv"] + sb["kv_unique"]) / (main["dec_ms"] * 1e-3) / 1e9, 1)
+    if "e2e_ms" in main:
+        res = main["res"]
+        line["e2e"] = {"value": round(world * sb["step"] / (main["e2e_ms"] * 1e-3) / 1e9, 2),
+                       "unit": "GB/s", "ms_per_step": round(main["e2e_ms"], 5),
+                       "h2d_bytes_per_step": res.h2d_bytes, "d2h_bytes_per_step": res.d2h_bytes}
+    if MIXED_CONFIG in result and MIXED_CONFIG != args.config:
+        m = result[MIXED_CONFIG]
+        mw = m["w"]
+        line["mixed_batch"] = {
+            "workload": f"{wl.CONFIG_NAMES[MIXED_CONFIG]}: {wl.CONFIG_DESCRIPTIONS[MIXED_CONFIG]}",
+            "value": round(world * mw.num_tokens / (m["ms"] * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(m["ms"], 5), "steps": m["steps"],
+            "attention_kernel_ms": round(m["dec_ms"], 5),
+            "kv_bytes": m["sb"]["kv"], "prefill_causal_flops": prefill_flops(mw)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arms
+# ---------------------------------------------------------------------------
+def _oracle_sample(w: wl.Workload, reqs, threads):
+    import oracle
+    kc, vc = w.k_cache, w.v_cache
+    oracle.write_kv(w.k_new, w.v_new, w.slot_mapping, kc, vc)
+    oracle.attention(w.q, kc, vc, w.block_tables, w.seq_lens, w.query_start_loc, w.scale,
+                     reqs=reqs, threads=threads)
+
+
+def _sample_bytes(w: wl.Workload, reqs) -> int:
+    sub = wl.subset_requests(w, reqs)
+    return step_bytes(sub)["step"]
+
+
+def cpu_baseline(w: wl.Workload, seconds: float) -> dict:
+    """The oracle as it stands on the host cores, on whole requests of the
+    workload taken in order until `seconds` of work is done."""
+    threads = os.cpu_count() or 1
+    done_bytes, t0, r, reqs_done = 0, time.perf_counter(), 0, 0
+    while time.perf_counter() - t0 < seconds and reqs_done < 100000:
+        batch = [(r + i) % w.num_reqs for i in range(min(8, w.num_reqs))]
+        _oracle_sample(w, batch, threads)
+        done_bytes += _sample_bytes(w, batch)
+        r = (r + len(batch)) % w.num_reqs
+        reqs_done += len(batch)
+    el = time.perf_counter() - t0
+    return {"value": round(done_bytes / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reqs_done} requests of {w.name} (8 at a time, in order) in {el:.1f} s, "
+                      f"write + attention, float64"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = wl.make_config(args.config)
+    threads = os.cpu_count() or 1
+    times, sizes = [], []
+    for i in range(args.warmup + args.steps):
+        req = [i % w.num_reqs]
+        t0 = time.perf_counter()
+        _oracle_sample(w, req, threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            sizes.append(_sample_bytes(w, req))
+    tot = sum(times)
+    value = sum(sizes) / tot / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot / len(times), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.CONFIG_NAMES[args.config]}: "
+                               f"{wl.CONFIG_DESCRIPTIONS[args.config]}",
+                   "sample": "one request of the batch per step (write + attention)"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": "one request of the workload per step, in order"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=HEADLINE_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local, dist = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * pa_api.h - C ABI of libpagedattn: attention over a paged KV cache on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Two operations make up the path:
+ *
+ *   pa_write_kv   scatters each new token's K and V rows into its physical
+ *                 cache slot through a slot mapping ("vLLM v1 Deep Dive: How
+ *                 LLM(...) and the Server Boot and Generate", Part 3, "Aside -
+ *                 KV cache and prefix caching": a slot is
+ *                 block_id * block_size + offset and a scatter kernel writes
+ *                 the freshly computed K/V there; "vLLM: An Exhaustive
+ *                 Technical Study for Kernel Engineers", 2.1, "Reaching the
+ *                 kernel").
+ *
+ *   pa_attention  runs attention for a unified mixed batch in one call:
+ *                 prefill-chunk query spans attend causally over [their cached
+ *                 prefix + their own new tokens], single-token decodes attend
+ *                 over all of their blocks, every request reading K/V through
+ *                 its own block table (same Aside, the block_table paragraph;
+ *                 same page, Part 3, "Step 4c - Mixed batches" for
+ *                 query_start_loc; "vLLM: An Exhaustive Technical Study for
+ *                 Kernel Engineers", 2.4, "The seam" and "The backend
+ *                 abstraction").
+ *
+ * Conventions shared by every call
+ *  - All tensor arguments are DEVICE pointers owned by the caller. The library
+ *    never allocates, frees or synchronises inside pa_write_kv/pa_attention;
+ *    work is enqueued on `stream` (a cudaStream_t, or NULL for the legacy
+ *    default stream) and the call returns at once.
+ *  - Element type of q, k, v, k_cache, v_cache and out: bfloat16, passed as
+ *    raw 16-bit storage. Index tensors: slot_mapping int64, the rest int32.
+ *  - Layouts (row-major, contiguous):
+ *      q, out            [num_tokens][num_q_heads][head_dim]
+ *      k, v              [num_tokens][num_kv_heads][head_dim]
+ *      k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]
+ *                        (one (block, kv head) is a contiguous block_size x
+ *                        head_dim tile: the head-major "HND" block layout,
+ *                        which "vLLM: An Exhaustive Technical Study for Kernel
+ *                        Engineers", 2.6, names as the default for non-MLA
+ *                        models)
+ *      block_tables      [num_reqs][max_blocks_per_req]
+ *      seq_lens          [num_reqs]
+ *      query_start_loc   [num_reqs + 1], query_start_loc[0] == 0, non-decreasing
+ *  - Supported shapes: block_size == 16; head_dim 64 or 128;
+ *    num_q_heads / num_kv_heads (the GQA group) in {1, 2, 4, 8}. Other values
+ *    return PA_ERR_UNSUPPORTED before anything is launched.
+ *  - Every device pointer must be 16-byte aligned (PA_ERR_INVALID_ARG).
+ *  - Errors that need the data to detect (a slot or block id outside the pool,
+ *    seq_len shorter than the query span) are caught by the kernels: the bad
+ *    item is skipped and a device error word is set, to be read with
+ *    pa_get_device_error. Nothing traps and nothing waits unboundedly; a
+ *    bounded wait that gives up reports PA_ERR_TIMEOUT the same way.
+ *  - The first call on a device performs a one-time set-up (device property
+ *    query and the address of the device error word); make one call, or
+ *    pa_init, before capturing a stream into a CUDA graph.
+ */
+#ifndef PA_API_H
+#define PA_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1, /* null pointer, negative size, misaligned pointer, bad shape */
+  PA_ERR_UNSUPPORTED = -2, /* block_size, head_dim or GQA group outside the supported set */
+  PA_ERR_WORKSPACE = -3,   /* workspace null or smaller than pa_attention_workspace_size */
+  PA_ERR_CUDA = -4,        /* a CUDA runtime call or a launch failed */
+  PA_ERR_BOUNDS = -5,      /* (device error word) an index was outside its valid range */
+  PA_ERR_TIMEOUT = -6      /* (device error word) a bounded wait in a kernel gave up */
+} pa_status;
+
+/* Device error word codes (pa_get_device_error `code`). */
+#define PA_DEVERR_NONE 0
+#define PA_DEVERR_SLOT 1         /* pa_write_kv: slot_mapping[t] >= num_blocks * block_size */
+#define PA_DEVERR_BLOCK_ID 2     /* pa_attention: a block table entry outside [0, num_blocks) */
+#define PA_DEVERR_LENGTHS 3      /* pa_attention: seq_len < query span, or too many blocks */
+#define PA_DEVERR_QSL 4          /* pa_attention: query_start_loc not within [0, num_tokens] */
+#define PA_DEVERR_WAIT_TIMEOUT 5 /* a kernel's bounded wait on a copy gave up */
+
+/*
+ * One-time per-device set-up for the current device (see the conventions).
+ * Idempotent; the other calls do it on first use.
+ */
+pa_status pa_init(void);
+
+/*
+ * Scatter new K/V rows into the paged caches.
+ *   k, v           [num_tokens][num_kv_heads][head_dim] bf16, read only
+ *   slot_mapping   [num_tokens] int64; token t goes to block
+ *                  slot_mapping[t] / block_size, row slot_mapping[t] % block_size.
+ *                  A negative slot marks a padding token: it is skipped.
+ *   k_cache, v_cache  written at the named slots only; every other slot keeps
+ *                  its contents, bit for bit.
+ * Copies are exact (bit patterns). Two tokens naming the same slot is the
+ * caller's error; which one lands is unspecified. A slot >= num_blocks *
+ * block_size is skipped and sets PA_DEVERR_SLOT.
+ * head_dim here may be any multiple of 8 (the scatter is type-agnostic).
+ */
+pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
+                      void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+                      int head_dim, int block_size, int num_blocks, void* stream);
+
+/*
+ * Bytes of device workspace pa_attention needs for a batch of this size
+ * (planner output, split-KV partial results and merge counters). The value
+ * depends only on the arguments, not on the device. Returns 0 on bad
+ * arguments.
+ */
+size_t pa_attention_workspace_size(int num_reqs, int num_tokens, int num_q_heads,
+                                   int num_kv_heads, int head_dim);
+
+/*
+ * Attention for a mixed batch of decodes and prefill chunks.
+ *   q                [num_tokens][num_q_heads][head_dim] bf16
+ *   k_cache, v_cache the pool, already holding this step's new K/V
+ *                    (call pa_write_kv first, on the same stream)
+ *   block_tables     request r's logical block i is physical block
+ *                    block_tables[r][i]; entries past ceil(seq_lens[r] / 16)
+ *                    are never read
+ *   seq_lens         total KV length of each request, new tokens included
+ *   query_start_loc  request r's new tokens are rows
+ *                    query_start_loc[r] .. query_start_loc[r+1]-1 of q/out;
+ *                    with qlen = that count and ctx = seq_lens[r] - qlen, row
+ *                    j attends to keys 0 .. ctx + j (causal, bottom-right
+ *                    aligned; a decode is qlen 1 and sees every key)
+ *   scale            multiplies q.k before the softmax (usually 1/sqrt(head_dim))
+ *   out              [num_tokens][num_q_heads][head_dim] bf16; rows of
+ *                    requests with qlen 0 and rows past query_start_loc[num_reqs]
+ *                    are left untouched
+ *   query head h reads KV head h / (num_q_heads / num_kv_heads)
+ *   max_blocks_per_req  row stride of block_tables
+ *   max_query_len, max_seq_len  host-side upper bounds the scheduler already
+ *                    knows; they only size launches (max_query_len <= 1 skips
+ *                    the prefill-chunk kernel). Values below the true maxima
+ *                    are an error (PA_DEVERR_LENGTHS).
+ *   workspace        device buffer of at least
+ *                    pa_attention_workspace_size(...) bytes, 256-byte aligned,
+ *                    no initial contents required; it must not be used by
+ *                    another call that runs concurrently on the GPU.
+ */
+pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, float scale, void* out, int num_reqs,
+                       int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, int max_blocks_per_req,
+                       int max_query_len, int max_seq_len, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a pa_status value (static string). */
+const char* pa_status_string(int status);
+
+/*
+ * Read the current device's error word: *code gets a PA_DEVERR_* value,
+ * *detail the offending index (token, request or block position). With
+ * clear != 0 the word is reset. Synchronises the device; not for the hot path.
+ * Either output pointer may be NULL.
+ */
+pa_status pa_get_device_error(int* code, long long* detail, int clear);
+
+/*
+ * Instrumentation: record `start_event` / `stop_event` (cudaEvent_t handles
+ * created by the caller) around every later launch of the given kernel on its
+ * stream; pass NULL events to stop. Kernel ids: 0 write_kv, 1 planner,
+ * 2 decode (split-KV), 3 prefill chunk. Process-wide setting, not thread-safe.
+ */
+pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event);
+
+/* Number of kernel launches the library has issued in this process. */
+long long pa_launch_count(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_API_H */

@@ -1,0 +1,700 @@
+// Planner and split-KV paged attention for one query token per work unit.
+//
+// What is computed ("vLLM v1 Deep Dive: How LLM(...) and the Server Boot and
+// Generate", Part 3, "Step 4c - Mixed batches" and "Aside - KV cache and
+// prefix caching"): for every new token of the batch, softmax attention of
+// each of its query heads over the keys the token may see - all of a decode
+// request's keys, or keys 0 .. ctx + j for token j of a prefill chunk on top
+// of ctx cached tokens - with K/V reached through the request's block table.
+// Query heads that share a KV head are processed together so each K/V block
+// is read once per KV head ("vLLM: An Exhaustive Technical Study for Kernel
+// Engineers", 2.4, the GQA grouping of the Triton unified attention backend).
+//
+// Work decomposition (ours). The planner lists every token with work and the
+// number of (kv head, 16-key block) items it needs; all items of all tokens
+// form one flattened sequence, token-major, then kv head, then block. The
+// decode grid is persistent (a multiple of the SM count) and each warp is an
+// independent worker that takes one contiguous, equally sized slice of that
+// sequence, so the load balance is exact whatever the length mix. A warp
+// whose slice holds a whole (token, kv head) writes the output directly;
+// otherwise it writes an unnormalised partial (o, m, l) and the last warp to
+// finish that (token, kv head) merges the partials by log-sum-exp
+// renormalisation ("vLLM: An Exhaustive Technical Study for Kernel
+// Engineers", 2.3, cascade attention's log-sum-exp merge) - no second kernel,
+// no spin-wait, a fixed merge order (deterministic results).
+//
+// Data movement. Each (block, kv head) of K and of V is one contiguous
+// 16 x D bf16 tile in the cache, fetched whole with a 1-D bulk async copy
+// (TMA) into a per-warp ring of shared-memory stages, completion tracked by
+// an mbarrier; NSTAGE-1 tiles are in flight while one is consumed. The q rows
+// of a (token, kv head) ride along with its first tile. Block ids are
+// prefetched 32 positions ahead with one coalesced load per warp.
+//
+// Arithmetic. Scores in fp32 with packed fp32x2 FMAs; q is prescaled by
+// scale*log2(e) so the online softmax uses exp2. Per-token dot products are
+// split over TPT lanes and reduced with a transposing butterfly of warp
+// shuffles (G heads -> 1 value per lane in log2(TPT) shuffle rounds).
+#include <math.h>
+
+#include "pa_internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// =============================================================================
+// Planner: one CTA. Writes the compacted unit list, the flattened positions
+// (prefix sum) and zeroes the merge counters.
+// =============================================================================
+constexpr int kPlanThreads = 1024;
+
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* total,
+                                                          long long* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long s = lane < nw ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(kFull, s, o);
+      if (lane >= o) s += y;
+    }
+    sm[lane] = s;
+  }
+  __syncthreads();
+  const long long before = warp ? sm[warp - 1] : 0;
+  *total = sm[nw - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
+  // The decode grid may be scheduled now; it waits for this grid to finish
+  // before reading the plan.
+  griddep_launch_dependents();
+  __shared__ long long scan_sm[32];
+  const int T = p.num_tokens;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) p.units[t] = UnitInfo{t, -1, 0, 0};
+  __syncthreads();
+  for (int r = threadIdx.x; r < p.num_reqs; r += blockDim.x) {
+    const int q0 = p.qsl[r], q1 = p.qsl[r + 1];
+    if (q0 < 0 || q1 < q0 || q1 > T) {
+      report_error(p.err, PA_DEVERR_QSL, r);
+      continue;
+    }
+    const int qlen = q1 - q0, L = p.seq_lens[r];
+    if (L < qlen || (L + kBlockSize - 1) / kBlockSize > p.max_blocks_per_req ||
+        qlen > p.max_query_len || L > p.max_seq_len) {
+      report_error(p.err, PA_DEVERR_LENGTHS, r);
+      continue;
+    }
+    const int ctx = L - qlen;
+    for (int j = 0; j < qlen; ++j) p.units[q0 + j] = UnitInfo{q0 + j, r, ctx + j + 1, 0};
+  }
+  __syncthreads();
+  constexpr long long kLow = (1LL << 40) - 1;
+  long long run_k = 0, run_w = 0;
+  for (int c0 = 0; c0 < T; c0 += blockDim.x) {
+    const int t = c0 + threadIdx.x;
+    const UnitInfo u = t < T ? p.units[t] : UnitInfo{0, -1, 0, 0};
+    const int nb = (u.len + kBlockSize - 1) / kBlockSize;
+    const long long packed = ((long long)(nb > 0) << 40) | ((long long)nb * p.num_kv_heads);
+    long long total;
+    const long long ex = block_exclusive_scan(packed, &total, scan_sm);
+    if (nb > 0) p.units[run_k + (ex >> 40)] = UnitInfo{u.tok, u.req, u.len, (int)(run_w + (ex & kLow))};
+    run_k += total >> 40;
+    run_w += total & kLow;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    p.units[run_k] = UnitInfo{T, -1, 0, (int)run_w};  // base[K] = W
+    p.header->num_units = (int)run_k;
+    p.header->num_positions = (int)run_w;
+  }
+  for (long long i = threadIdx.x; i < run_k * p.num_kv_heads; i += blockDim.x) p.counters[i] = 0;
+}
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
+  pa_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// =============================================================================
+// Split-KV decode kernel
+// =============================================================================
+template <int D, int G>
+struct Cfg {
+  static constexpr int DPT = (G <= 4) ? 16 : 8;  // q.k dims per lane
+  static constexpr int TPT = D / DPT;            // lanes per token in q.k
+  static constexpr int TPP = 32 / TPT;           // tokens per q.k pass
+  static constexpr int NPASS = 16 / TPP;
+  static constexpr int LOG_G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  static constexpr int LPR = D / 4;   // lanes per V row (4 dims each)
+  static constexpr int RPS = 32 / LPR;  // V rows per step
+  static constexpr int KV_BYTES = kBlockSize * D * 2;
+  static constexpr int Q_BYTES = G * D * 2;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
+  static constexpr int P_BYTES = kBlockSize * G * 4 + 64;  // p[16][G] then alpha[G]
+  static_assert(TPT >= G, "a token's lane group must hold one value per head");
+  static_assert(DPT == 8 || DPT == 16, "one or two 16-byte chunks per lane");
+};
+
+template <int D, int G, int NSTAGE>
+struct WarpSmem {
+  using C = Cfg<D, G>;
+  static constexpr int RAW = NSTAGE * C::STAGE_BYTES + C::P_BYTES + NSTAGE * 8;
+  static constexpr int BYTES = (RAW + 127) / 128 * 128;
+};
+
+// Head whose score a lane holds after the transposing reduction.
+template <int G>
+__device__ __forceinline__ int head_of_lane(int lane) {
+  int h = 0;
+#pragma unroll
+  for (int st = 0; (1 << st) < G; ++st) h += ((lane >> st) & 1) * (G >> (st + 1));
+  return h;
+}
+template <int G>
+__device__ __forceinline__ int lane_of_head(int h) {
+  constexpr int LOG_G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  int lane = 0;
+#pragma unroll
+  for (int st = 0; st < LOG_G; ++st) lane |= ((h >> (LOG_G - 1 - st)) & 1) << st;
+  return lane;
+}
+
+// Sum G per-lane partial dot products over the TPT lanes of a token group.
+// Each round halves the number of live values: a lane keeps one half, sends
+// the other to its partner and adds what it receives. Ends with the full sum
+// for head head_of_lane<G>(lane) in every lane of the group.
+template <int G, int TPT>
+__device__ __forceinline__ float reduce_heads(float (&v)[G], int lane) {
+#pragma unroll
+  for (int st = 0; (1 << st) < TPT; ++st) {
+    const int m = 1 << st;
+    const int n = (G >> st) > 1 ? (G >> st) : 1;
+    if (n > 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = upper ? v[i] : v[i + n / 2];
+        const float keep = upper ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(kFull, send, m);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(kFull, v[0], m);
+    }
+  }
+  return v[0];
+}
+
+// Per-lane metadata of one position of a 32-position batch.
+struct Batch {
+  int k, tok, len, kv, blk, nb, pid, end;
+};
+struct Loc {
+  int k, tok, req, len, base;
+};
+
+template <int D, int G, int WARPS, int NSTAGE>
+__global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParams p) {
+  using C = Cfg<D, G>;
+  using WS = WarpSmem<D, G, NSTAGE>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t stage0 = smem_u32(smem + warp * WS::BYTES);
+  const uint32_t p_s = stage0 + NSTAGE * C::STAGE_BYTES;
+  const uint32_t alpha_s = p_s + kBlockSize * G * 4;
+  const uint32_t bars = p_s + C::P_BYTES;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(bars + 8 * s, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  griddep_wait();  // the plan is written by the preceding grid
+
+  const int W = p.header->num_positions;
+  const int K = p.header->num_units;
+  if (W <= 0) return;
+  const int NW_all = gridDim.x * WARPS;
+  int NW = W / 8;  // at least 8 positions per worker
+  NW = NW < 1 ? 1 : (NW > NW_all ? NW_all : NW);
+  const int w = blockIdx.x * WARPS + warp;
+  if (w >= NW) return;
+  const int S = (int)((long long)w * W / NW);
+  const int E = (int)((long long)(w + 1) * W / NW);
+  if (S >= E) return;
+  const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
+
+  auto worker_of = [&](int x) -> int { return (int)(((long long)(x + 1) * NW - 1) / W); };
+
+  // ---- batch metadata helpers ------------------------------------------------
+  auto window = [&](int kbase) -> int {
+    const int kk = kbase + lane;
+    return kk <= K ? __ldg(&p.units[kk].base) : 0x7fffffff;
+  };
+  auto locate = [&](int y0, int kbase, int win) -> Loc {
+    const int y = y0 + lane;
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) c += (__shfl_sync(kFull, win, i) <= y) ? 1 : 0;
+    int k = kbase + c - 1;
+    k = k < 0 ? 0 : (k > K ? K : k);
+    const int4 u = __ldg(reinterpret_cast<const int4*>(p.units) + k);
+    return Loc{k, u.x, u.y, u.z, u.w};
+  };
+  auto finish = [&](int y0, const Loc& kl) -> Batch {
+    Batch b;
+    const int y = y0 + lane;
+    b.k = kl.k;
+    b.tok = kl.tok;
+    b.len = kl.len;
+    const int base = kl.base;
+    int nb = (b.len + kBlockSize - 1) / kBlockSize;
+    nb = nb < 1 ? 1 : nb;
+    b.nb = nb;
+    b.end = base + nb * Hkv;
+    const int off = y - base;
+    b.kv = off / nb;
+    b.blk = off - b.kv * nb;
+    int pid = 0;
+    if (y < E) {
+      pid = __ldg(p.block_tables + (size_t)kl.req * p.bt_stride + b.blk);
+      if (pid < 0 || pid >= p.num_blocks) {
+        report_error(p.err, PA_DEVERR_BLOCK_ID, y);
+        pid = 0;
+      }
+    }
+    b.pid = pid;
+    return b;
+  };
+
+  // ---- locate the first position: 32-ary search over units[].base --------------
+  int lo = 0, hi = K;  // base[lo] <= S < base[hi]
+#pragma unroll 1
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool ok = idx < hi && __ldg(&p.units[idx].base) <= S;
+    const unsigned bal = __ballot_sync(kFull, ok);
+    const int last = 31 - __clz(bal);
+    lo = lo + last * step;
+    hi = min(hi, lo + step);
+  }
+
+  Batch cur = finish(S, locate(S, lo, window(lo)));
+  Batch nxt = cur;
+  int y0 = S;
+  int nwin = 0, nkbase = 0;
+  Loc nkl{0, 0, 0, 0, 0};
+
+  auto issue = [&](int stage, int pid, int kv, bool with_q, int tok) {
+    if (lane == 0) {
+      const uint32_t dst = stage0 + stage * C::STAGE_BYTES;
+      const uint32_t bar = bars + 8 * stage;
+      const size_t off = ((size_t)pid * Hkv + kv) * (kBlockSize * D);
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, 2 * C::KV_BYTES + (with_q ? C::Q_BYTES : 0));
+      bulk_g2s(dst, p.k_cache + off, C::KV_BYTES, bar);
+      bulk_g2s(dst + C::KV_BYTES, p.v_cache + off, C::KV_BYTES, bar);
+      if (with_q)
+        bulk_g2s(dst + 2 * C::KV_BYTES, p.q + ((size_t)tok * Hq + (size_t)kv * G) * D, C::Q_BYTES,
+                 bar);
+    }
+  };
+
+  // prologue
+#pragma unroll
+  for (int i = 0; i < NSTAGE; ++i) {
+    if (S + i < E) {
+      const int pid = __shfl_sync(kFull, cur.pid, i);
+      const int kv = __shfl_sync(kFull, cur.kv, i);
+      const int blk = __shfl_sync(kFull, cur.blk, i);
+      const int tok = __shfl_sync(kFull, cur.tok, i);
+      issue(i, pid, kv, i == 0 || blk == 0, tok);
+    }
+  }
+
+  // ---- per-lane roles ---------------------------------------------------------------
+  const int sub = lane % C::TPT;                                 // q.k dim slice
+  const int tg = lane / C::TPT;                                  // token within a pass
+  const int swz = (C::DPT == 16) ? ((lane >> 2) & 1) : 0;        // bank-conflict-free order
+  const int hsel = head_of_lane<G>(lane);
+  const int rl = lane % C::LPR;                                  // V dims 4*rl .. 4*rl+3
+  const int rrow = lane / C::LPR;                                // V row within a step
+
+  float2 qv[G][C::DPT / 2];
+  float2 acc[G][2];
+  float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    acc[h][0] = make_float2(0.f, 0.f);
+    acc[h][1] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < C::DPT / 2; ++i) qv[h][i] = make_float2(0.f, 0.f);
+  }
+
+  int stage = 0;
+  uint32_t phase = 0;
+#pragma unroll 1
+  for (int y = S; y < E; ++y) {
+    int j = y - y0;
+    if (j == 32) {
+      cur = nxt;
+      y0 += 32;
+      j = 0;
+    }
+    if (y0 + 32 < E) {  // stage the metadata of the next batch, a step at a time
+      if (j == 0) {
+        const int k31 = __shfl_sync(kFull, cur.k, 31);
+        const int end31 = __shfl_sync(kFull, cur.end, 31);
+        nkbase = (y0 + 32 >= end31) ? k31 + 1 : k31;
+        nwin = window(nkbase);
+      } else if (j == 8) {
+        nkl = locate(y0 + 32, nkbase, nwin);
+      } else if (j == 16) {
+        nxt = finish(y0 + 32, nkl);
+      }
+    }
+    const int kk = __shfl_sync(kFull, cur.k, j);
+    const int tok = __shfl_sync(kFull, cur.tok, j);
+    const int len = __shfl_sync(kFull, cur.len, j);
+    const int kv = __shfl_sync(kFull, cur.kv, j);
+    const int blk = __shfl_sync(kFull, cur.blk, j);
+    const int nb = __shfl_sync(kFull, cur.nb, j);
+    const bool seg_start = (y == S) || blk == 0;
+    const bool seg_end = (y == E - 1) || blk == nb - 1;
+    const uint32_t st_base = stage0 + stage * C::STAGE_BYTES;
+    const uint32_t bar = bars + 8 * stage;
+
+    if (!mbar_wait_bounded(bar, phase)) {
+      if (lane == 0) report_error(p.err, PA_DEVERR_WAIT_TIMEOUT, y);
+      // let every copy still in flight land before the CTA can exit
+      int st2 = stage;
+      uint32_t ph2 = phase;
+      for (int y2 = y; y2 < E && y2 < y + NSTAGE; ++y2) {
+        mbar_wait_bounded(bars + 8 * st2, ph2);
+        if (++st2 == NSTAGE) { st2 = 0; ph2 ^= 1; }
+      }
+      return;
+    }
+
+    if (seg_start) {
+      const uint32_t qbase = st_base + 2 * C::KV_BYTES;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const uint32_t row = qbase + h * D * 2 + sub * C::DPT * 2;
+        const uint4 a = lds128(row + 16 * swz);
+        qv[h][0] = bf16x2_to_float2(a.x);
+        qv[h][1] = bf16x2_to_float2(a.y);
+        qv[h][2] = bf16x2_to_float2(a.z);
+        qv[h][3] = bf16x2_to_float2(a.w);
+        if constexpr (C::DPT == 16) {
+          const uint4 b = lds128(row + 16 * (1 - swz));
+          qv[h][4] = bf16x2_to_float2(b.x);
+          qv[h][5] = bf16x2_to_float2(b.y);
+          qv[h][6] = bf16x2_to_float2(b.z);
+          qv[h][7] = bf16x2_to_float2(b.w);
+        }
+#pragma unroll
+        for (int i = 0; i < C::DPT / 2; ++i)
+          qv[h][i] = fmul2(qv[h][i], make_float2(p.scale_log2, p.scale_log2));
+        acc[h][0] = make_float2(0.f, 0.f);
+        acc[h][1] = make_float2(0.f, 0.f);
+      }
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+
+    const int nvalid = min(kBlockSize, len - blk * kBlockSize);
+
+    // ---- scores: s = (q * scale * log2 e) . k for the lane's (head, token) ---------
+    float sc[C::NPASS];
+#pragma unroll
+    for (int ps = 0; ps < C::NPASS; ++ps) {
+      const int t = ps * C::TPP + tg;
+      const uint32_t row = st_base + t * D * 2 + sub * C::DPT * 2;
+      float2 kf[C::DPT / 2];
+      {
+        const uint4 a = lds128(row + 16 * swz);
+        kf[0] = bf16x2_to_float2(a.x);
+        kf[1] = bf16x2_to_float2(a.y);
+        kf[2] = bf16x2_to_float2(a.z);
+        kf[3] = bf16x2_to_float2(a.w);
+        if constexpr (C::DPT == 16) {
+          const uint4 b = lds128(row + 16 * (1 - swz));
+          kf[4] = bf16x2_to_float2(b.x);
+          kf[5] = bf16x2_to_float2(b.y);
+          kf[6] = bf16x2_to_float2(b.z);
+          kf[7] = bf16x2_to_float2(b.w);
+        }
+      }
+      float part[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float2 a2 = fmul2(qv[h][0], kf[0]);
+#pragma unroll
+        for (int i = 1; i < C::DPT / 2; ++i) a2 = ffma2(qv[h][i], kf[i], a2);
+        part[h] = a2.x + a2.y;
+      }
+      const float s = reduce_heads<G, C::TPT>(part, lane);
+      sc[ps] = (t < nvalid) ? s : -INFINITY;
+    }
+
+    // ---- online softmax (base 2) ------------------------------------------------------
+    float mb = sc[0];
+#pragma unroll
+    for (int ps = 1; ps < C::NPASS; ++ps) mb = fmaxf(mb, sc[ps]);
+#pragma unroll
+    for (int o = C::TPT; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+    const float m_new = fmaxf(m_run, mb);
+    const float alpha = exp2f(m_run - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int ps = 0; ps < C::NPASS; ++ps) {
+      const float pr = exp2f(sc[ps] - m_new);
+      psum += pr;
+      const int t = ps * C::TPP + tg;
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(p_s + (t * G + hsel) * 4), "f"(pr) : "memory");
+    }
+    l_run = l_run * alpha + psum;
+    m_run = m_new;
+    if (lane < G)
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(alpha_s + hsel * 4), "f"(alpha) : "memory");
+    __syncwarp();
+
+    // ---- o = o * alpha + sum_t p_t v_t ---------------------------------------------------
+    {
+      float al[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(al[h]) : "r"(alpha_s + h * 4));
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        acc[h][0] = fmul2(acc[h][0], make_float2(al[h], al[h]));
+        acc[h][1] = fmul2(acc[h][1], make_float2(al[h], al[h]));
+      }
+#pragma unroll
+      for (int stp = 0; stp < kBlockSize / C::RPS; ++stp) {
+        const int t = stp * C::RPS + rrow;
+        if (t < nvalid) {
+          const uint2 vv = lds64(st_base + C::KV_BYTES + t * D * 2 + rl * 8);
+          const float2 v01 = bf16x2_to_float2(vv.x);
+          const float2 v23 = bf16x2_to_float2(vv.y);
+          float pp[G];
+          if constexpr (G >= 4) {
+#pragma unroll
+            for (int h4 = 0; h4 < G; h4 += 4) {
+              const uint4 q4 = lds128(p_s + (t * G + h4) * 4);
+              pp[h4 + 0] = __uint_as_float(q4.x);
+              pp[h4 + 1] = __uint_as_float(q4.y);
+              pp[h4 + 2] = __uint_as_float(q4.z);
+              pp[h4 + 3] = __uint_as_float(q4.w);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[h]) : "r"(p_s + (t * G + h) * 4));
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float2 ph = make_float2(pp[h], pp[h]);
+            acc[h][0] = ffma2(ph, v01, acc[h][0]);
+            acc[h][1] = ffma2(ph, v23, acc[h][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane is done with this stage and with p_s
+
+    // ---- refill this stage with the position NSTAGE ahead -----------------------------------
+    {
+      const int yi = y + NSTAGE;
+      if (yi < E) {
+        const int ji = yi - y0;
+        int pid, kvi, blki, toki;
+        if (ji < 32) {
+          pid = __shfl_sync(kFull, cur.pid, ji);
+          kvi = __shfl_sync(kFull, cur.kv, ji);
+          blki = __shfl_sync(kFull, cur.blk, ji);
+          toki = __shfl_sync(kFull, cur.tok, ji);
+        } else {
+          pid = __shfl_sync(kFull, nxt.pid, ji - 32);
+          kvi = __shfl_sync(kFull, nxt.kv, ji - 32);
+          blki = __shfl_sync(kFull, nxt.blk, ji - 32);
+          toki = __shfl_sync(kFull, nxt.tok, ji - 32);
+        }
+        issue(stage, pid, kvi, blki == 0, toki);
+      }
+    }
+    if (++stage == NSTAGE) {
+      stage = 0;
+      phase ^= 1;
+    }
+
+    if (seg_end) {
+      // complete row sums and gather (m, l) of every head into every lane
+      float lsum = l_run;
+#pragma unroll
+      for (int o = C::TPT; o < 32; o <<= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+      float mh[G], lh[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const int src = lane_of_head<G>(h);
+        mh[h] = __shfl_sync(kFull, m_run, src);
+        lh[h] = __shfl_sync(kFull, lsum, src);
+      }
+      if constexpr (C::RPS == 2) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          acc[h][0].x += __shfl_xor_sync(kFull, acc[h][0].x, 16);
+          acc[h][0].y += __shfl_xor_sync(kFull, acc[h][0].y, 16);
+          acc[h][1].x += __shfl_xor_sync(kFull, acc[h][1].x, 16);
+          acc[h][1].y += __shfl_xor_sync(kFull, acc[h][1].y, 16);
+        }
+      }
+      const int ustart = y - blk;  // first position of this (token, kv head)
+      const int wf = worker_of(ustart), wl = worker_of(ustart + nb - 1);
+      uint16_t* orow = p.out + ((size_t)tok * Hq + (size_t)kv * G) * D + rl * 4;
+      if (wf == wl) {
+        if (rrow == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float inv = 1.f / lh[h];
+            uint2 pk;
+            pk.x = float2_to_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
+            pk.y = float2_to_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
+            *reinterpret_cast<uint2*>(orow + h * D) = pk;
+          }
+        }
+      } else {
+        const int u = kk * Hkv + kv;
+        float* slot = p.partials + (size_t)(u + w) * p.slot_floats;
+        if (lane == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            __stcg(slot + h, mh[h]);
+            __stcg(slot + G + h, lh[h]);
+          }
+        }
+        if (rrow == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            __stcg(reinterpret_cast<float4*>(slot + 16 + h * D + rl * 4),
+                   make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y));
+        }
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0) prev = atomicAdd(p.counters + u, 1);
+        prev = __shfl_sync(kFull, prev, 0);
+        if (prev == wl - wf) {  // every other segment has landed: merge them all
+          __threadfence();
+          float M[G], Ls[G];
+          float4 O[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            M[h] = -INFINITY;
+            Ls[h] = 0.f;
+            O[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll 1
+          for (int s = wf; s <= wl; ++s) {
+            const float* sl = p.partials + (size_t)(u + s) * p.slot_floats;
+#pragma unroll
+            for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(sl + h));
+          }
+#pragma unroll 1
+          for (int s = wf; s <= wl; ++s) {
+            const float* sl = p.partials + (size_t)(u + s) * p.slot_floats;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float f = exp2f(__ldcg(sl + h) - M[h]);
+              Ls[h] += __ldcg(sl + G + h) * f;
+              const float4 o = __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D + rl * 4));
+              O[h].x += o.x * f;
+              O[h].y += o.y * f;
+              O[h].z += o.z * f;
+              O[h].w += o.w * f;
+            }
+          }
+          if (rrow == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float inv = 1.f / Ls[h];
+              uint2 pk;
+              pk.x = float2_to_bf16x2(O[h].x * inv, O[h].y * inv);
+              pk.y = float2_to_bf16x2(O[h].z * inv, O[h].w * inv);
+              *reinterpret_cast<uint2*>(orow + h * D) = pk;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---- launch ---------------------------------------------------------------------------
+template <int D, int G, int WARPS, int NSTAGE>
+cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, cudaStream_t s) {
+  auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE>;
+  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE>::BYTES;
+  static int occ_cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int occ = (dev >= 0 && dev < 64) ? occ_cache[dev] : 0;
+  if (occ == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, WARPS * 32, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    if (dev >= 0 && dev < 64) occ_cache[dev] = occ;
+  }
+  int grid = num_sms * occ;
+  if (grid * WARPS > kMaxDecodeWorkers) grid = kMaxDecodeWorkers / WARPS;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
+                          cudaStream_t s) {
+  if (head_dim == 128) {
+    switch (group) {
+      case 1: return launch_decode_t<128, 1, 4, 3>(p, num_sms, s);
+      case 2: return launch_decode_t<128, 2, 4, 3>(p, num_sms, s);
+      case 4: return launch_decode_t<128, 4, 4, 3>(p, num_sms, s);
+      case 8: return launch_decode_t<128, 8, 3, 3>(p, num_sms, s);
+    }
+  } else if (head_dim == 64) {
+    switch (group) {
+      case 1: return launch_decode_t<64, 1, 4, 4>(p, num_sms, s);
+      case 2: return launch_decode_t<64, 2, 4, 4>(p, num_sms, s);
+      case 4: return launch_decode_t<64, 4, 4, 4>(p, num_sms, s);
+      case 8: return launch_decode_t<64, 8, 4, 4>(p, num_sms, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

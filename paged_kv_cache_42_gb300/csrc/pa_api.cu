@@ -1,0 +1,248 @@
+// C ABI of libpagedattn: argument validation, per-device set-up, the device
+// error word, optional launch timers and dispatch to the kernels.
+//
+// Validation happens before any CUDA call, so a malformed call is rejected
+// without touching (or needing) a GPU.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "pa_api.h"
+#include "pa_internal.h"
+
+namespace pa {
+
+// The device error word: [0] code (PA_DEVERR_*), [1] detail. One per device,
+// in static device memory; kernels receive its address as an argument.
+__device__ unsigned long long g_device_error[2];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned long long* err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+std::atomic<long long> g_launches{0};
+cudaEvent_t g_timer_start[4] = {nullptr, nullptr, nullptr, nullptr};
+cudaEvent_t g_timer_stop[4] = {nullptr, nullptr, nullptr, nullptr};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  DeviceState& d = g_devices[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!d.ready) {
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+      void* err = nullptr;
+      if (cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess) return PA_ERR_CUDA;
+      d.num_sms = sms;
+      d.err = static_cast<unsigned long long*>(err);
+      d.ready = true;
+    }
+  }
+  *out = &d;
+  return PA_OK;
+}
+
+struct TimerScope {
+  int id;
+  cudaStream_t s;
+  TimerScope(int kernel, cudaStream_t stream) : id(kernel), s(stream) {
+    if (g_timer_start[id]) cudaEventRecord(g_timer_start[id], s);
+  }
+  ~TimerScope() {
+    if (g_timer_stop[id]) cudaEventRecord(g_timer_stop[id], s);
+  }
+};
+
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+int pa_version(void) { return 100; }
+
+long long pa_launch_count(void) { return g_launches.load(); }
+
+const char* pa_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG: invalid argument";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: unsupported block_size / head_dim / group";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE: workspace missing or too small";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime or launch failure";
+    case PA_ERR_BOUNDS: return "PA_ERR_BOUNDS: index outside its valid range";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: a bounded device wait gave up";
+    default: return "unknown pa_status";
+  }
+}
+
+pa_status pa_init(void) {
+  DeviceState* d = nullptr;
+  return device_state(&d);
+}
+
+pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache,
+                      void* v_cache, int num_tokens, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0)
+    return PA_ERR_INVALID_ARG;
+  if (block_size != kBlockSize || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PA_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  if (pa_status st = device_state(&d)) return st;
+  WriteParams p;
+  p.k = static_cast<const uint16_t*>(k);
+  p.v = static_cast<const uint16_t*>(v);
+  p.slot_mapping = slot_mapping;
+  p.k_cache = static_cast<uint16_t*>(k_cache);
+  p.v_cache = static_cast<uint16_t*>(v_cache);
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.num_slots = (long long)num_blocks * kBlockSize;
+  p.err = d->err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  TimerScope timer(0, s);
+  const cudaError_t e = launch_write_kv(p, s);
+  g_launches.fetch_add(1);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_attention_workspace_size(int num_reqs, int num_tokens, int num_q_heads,
+                                   int num_kv_heads, int head_dim) {
+  if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0 || num_q_heads % num_kv_heads != 0)
+    return 0;
+  return ws_layout(num_tokens, num_q_heads, num_kv_heads, head_dim).total;
+}
+
+pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, float scale, void* out, int num_reqs,
+                       int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, int max_blocks_per_req,
+                       int max_query_len, int max_seq_len, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0 || num_blocks < 0 || max_blocks_per_req < 0 || max_query_len < 0 ||
+      max_seq_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128) ||
+      !supported_group(num_q_heads / num_kv_heads))
+    return PA_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN scale
+  if (num_reqs == 0 || num_tokens == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
+    return PA_ERR_INVALID_ARG;
+  // flattened work positions must fit a 32-bit int: tokens x Hkv x blocks per token
+  const long long max_blocks = ((long long)max_seq_len + kBlockSize - 1) / kBlockSize;
+  if ((long long)num_tokens * num_kv_heads * max_blocks >= (1LL << 31))
+    return PA_ERR_UNSUPPORTED;
+  const WsLayout lay = ws_layout(num_tokens, num_q_heads, num_kv_heads, head_dim);
+  if (!workspace || workspace_bytes < lay.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PA_ERR_WORKSPACE;
+
+  DeviceState* d = nullptr;
+  if (pa_status st = device_state(&d)) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+
+  PlanParams pp;
+  pp.qsl = query_start_loc;
+  pp.seq_lens = seq_lens;
+  pp.num_reqs = num_reqs;
+  pp.num_tokens = num_tokens;
+  pp.num_kv_heads = num_kv_heads;
+  pp.max_blocks_per_req = max_blocks_per_req;
+  pp.max_query_len = max_query_len;
+  pp.max_seq_len = max_seq_len;
+  pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
+  pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
+  pp.counters = reinterpret_cast<int*>(ws + lay.counters_off);
+  pp.err = d->err;
+  {
+    TimerScope timer(1, s);
+    const cudaError_t e = launch_plan(pp, s);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+
+  DecodeParams dp;
+  dp.q = static_cast<const uint16_t*>(q);
+  dp.k_cache = static_cast<const uint16_t*>(k_cache);
+  dp.v_cache = static_cast<const uint16_t*>(v_cache);
+  dp.block_tables = block_tables;
+  dp.out = static_cast<uint16_t*>(out);
+  dp.bt_stride = max_blocks_per_req;
+  dp.num_q_heads = num_q_heads;
+  dp.num_kv_heads = num_kv_heads;
+  dp.num_blocks = num_blocks;
+  dp.scale_log2 = scale * 1.4426950408889634f;
+  dp.header = pp.header;
+  dp.units = pp.units;
+  dp.counters = pp.counters;
+  dp.partials = reinterpret_cast<float*>(ws + lay.partials_off);
+  dp.slot_floats = lay.slot_floats;
+  dp.err = d->err;
+  {
+    TimerScope timer(2, s);
+    const cudaError_t e =
+        launch_decode(dp, head_dim, num_q_heads / num_kv_heads, d->num_sms, s);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+pa_status pa_get_device_error(int* code, long long* detail, int clear) {
+  DeviceState* d = nullptr;
+  if (pa_status st = device_state(&d)) return st;
+  unsigned long long w[2] = {0, 0};
+  if (cudaMemcpy(w, d->err, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  if (code) *code = (int)w[0];
+  if (detail) *detail = (long long)w[1];
+  if (clear) {
+    const unsigned long long z[2] = {0, 0};
+    if (cudaMemcpy(d->err, z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event) {
+  if (kernel_id < 0 || kernel_id >= 4) return PA_ERR_INVALID_ARG;
+  if ((start_event == nullptr) != (stop_event == nullptr)) return PA_ERR_INVALID_ARG;
+  g_timer_start[kernel_id] = static_cast<cudaEvent_t>(start_event);
+  g_timer_stop[kernel_id] = static_cast<cudaEvent_t>(stop_event);
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// Internal declarations shared by the translation units of libpagedattn.
+// Host and device code; no torch, no CUDA graph state.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_api.h"
+
+namespace pa {
+
+constexpr int kBlockSize = 16;
+// Upper bound on the number of split-KV decode workers (warps) of one launch.
+// The workspace reserves one partial-result slot per (token, kv head) plus one
+// per worker, so it is part of the workspace size formula.
+constexpr int kMaxDecodeWorkers = 4096;
+
+// One entry per token that has keys to attend to, in token order (the
+// planner compacts away tokens with no work). `base` is the first position
+// of the token's (kv head, block) sequence in the flattened decode work list.
+struct UnitInfo {
+  int tok;   // row of q / out
+  int req;   // request (row of block_tables)
+  int len;   // number of keys this token attends to (causal limit + 1)
+  int base;  // flattened position of (kv head 0, block 0)
+};
+static_assert(sizeof(UnitInfo) == 16, "UnitInfo is loaded as one 16-byte vector");
+
+struct WsHeader {
+  int num_units;      // K: tokens with work
+  int num_positions;  // W: sum over units of Hkv * ceil(len / 16)
+  int pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header occupies the first 256 bytes");
+
+// Workspace carve-up, identical on host and device.
+struct WsLayout {
+  size_t header_off, units_off, counters_off, partials_off, total;
+  int slot_floats;  // floats per partial-result slot
+};
+
+__host__ __device__ inline size_t pa_align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline WsLayout ws_layout(int num_tokens, int num_q_heads, int num_kv_heads,
+                                              int head_dim) {
+  WsLayout l;
+  const int G = num_q_heads / num_kv_heads;
+  l.slot_floats = 16 + G * head_dim;  // [m x G][l x G] padded to 16 floats, then o[G][D]
+  l.header_off = 0;
+  l.units_off = pa_align256(sizeof(WsHeader));
+  l.counters_off = l.units_off + pa_align256(sizeof(UnitInfo) * (size_t)(num_tokens + 1));
+  l.partials_off =
+      l.counters_off + pa_align256(sizeof(int) * (size_t)num_tokens * (size_t)num_kv_heads);
+  const size_t slots = (size_t)num_tokens * num_kv_heads + kMaxDecodeWorkers;
+  l.total = l.partials_off + pa_align256(sizeof(float) * (size_t)l.slot_floats * slots);
+  return l;
+}
+
+struct PlanParams {
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  int num_reqs, num_tokens, num_kv_heads, max_blocks_per_req, max_query_len, max_seq_len;
+  WsHeader* header;
+  UnitInfo* units;
+  int* counters;
+  unsigned long long* err;
+};
+
+struct DecodeParams {
+  const uint16_t* q;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  const int32_t* block_tables;
+  uint16_t* out;
+  int bt_stride, num_q_heads, num_kv_heads, num_blocks;
+  float scale_log2;  // scale * log2(e): scores are kept in base-2 exponent units
+  const WsHeader* header;
+  const UnitInfo* units;
+  int* counters;
+  float* partials;
+  int slot_floats;
+  unsigned long long* err;
+};
+
+struct WriteParams {
+  const uint16_t* k;
+  const uint16_t* v;
+  const int64_t* slot_mapping;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+  int num_tokens, num_kv_heads, head_dim;
+  long long num_slots;
+  unsigned long long* err;
+};
+
+// Device error word: [0] = code, [1] = detail. First error wins.
+__device__ inline void report_error(unsigned long long* err, int code, long long detail) {
+  if (atomicCAS(err, 0ull, (unsigned long long)code) == 0ull)
+    atomicExch(err + 1, (unsigned long long)detail);
+}
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s);
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+// grid_ctas is filled with the grid actually used. head_dim / G select the
+// instantiation; unsupported combinations return cudaErrorInvalidValue.
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
+                          cudaStream_t s);
+
+}  // namespace pa

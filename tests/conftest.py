@@ -17,3 +17,19 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(scope="session")
+def pa_lib():
+    """The product library (built in-tree if missing)."""
+    from paged_kv_cache_42_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def cuda_available() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
