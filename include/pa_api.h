@@ -152,6 +152,43 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        int max_query_len, int max_seq_len, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/*
+ * pa_attention without a caller-provided workspace, for callers that cannot
+ * allocate device memory (for example code running inside an allocator's own
+ * callbacks, or under a host framework that owns all device memory and offers
+ * no allocation hook). The pages describe no such entry point; it has no
+ * counterpart there.
+ *
+ * Arguments are those of pa_attention minus workspace / workspace_bytes; the
+ * caller still passes every input and output. The workspace is a fixed
+ * scratch array of PA_NOALLOC_SCRATCH_BYTES compiled into the library: each
+ * GPU that loads the library holds it until the process exits. The call
+ * allocates nothing (no cudaMalloc, no cudaFree, no library allocator).
+ *  - A batch whose pa_attention_workspace_size(...) exceeds
+ *    PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE before
+ *    anything is launched.
+ *  - The first call on a device looks up the scratch array's device address
+ *    (with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one scratch array, which keeps the
+ *    last call's contents; the kernels re-initialise everything they read
+ *    from it on each call. Calls whose work overlaps on the GPU (different
+ *    streams, or different host threads without ordering) race on the
+ *    scratch and give wrong results: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+pa_status pa_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, float scale, void* out,
+                               int num_reqs, int num_tokens, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_req, int max_query_len, int max_seq_len,
+                               void* stream);
+
+/* Size of the fixed scratch array used by pa_attention_noalloc. */
+size_t pa_noalloc_scratch_bytes(void);
+
 /* Human-readable name of a pa_status value (static string). */
 const char* pa_status_string(int status);
 

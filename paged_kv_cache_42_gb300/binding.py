@@ -183,3 +183,41 @@ def set_kernel_timer(kernel: str, start: torch.cuda.Event | None,
 
 def launch_count() -> int:
     return int(lib().pa_launch_count())
+
+
+def noalloc_scratch_bytes() -> int:
+    """Size of the fixed scratch array behind :func:`attention_noalloc`."""
+    L = lib()
+    L.pa_noalloc_scratch_bytes.argtypes = []
+    L.pa_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    return int(L.pa_noalloc_scratch_bytes())
+
+
+def attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                      query_start_loc: torch.Tensor, scale: float, *, max_query_len: int,
+                      max_seq_len: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """pa_attention_noalloc: attention with the library's fixed scratch array
+    as workspace, for callers that cannot allocate device memory.
+
+    Nothing is allocated by the call (``out`` must be given). Batches larger
+    than the scratch array raise PA_ERR_WORKSPACE; calls that overlap on the
+    GPU share the scratch and must be serialised by the caller.
+    """
+    L = lib()
+    L.pa_attention_noalloc.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, ctypes.c_float, _c_p,
+                                       _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
+                                       _c_i, _c_p]
+    L.pa_attention_noalloc.restype = _c_i
+    T, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    R = int(seq_lens.shape[0])
+    st = L.pa_attention_noalloc(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
+        _dev(seq_lens, torch.int32, "seq_lens"),
+        _dev(query_start_loc, torch.int32, "query_start_loc"), float(scale),
+        _dev(out, torch.bfloat16, "out"), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+        int(max_query_len), int(max_seq_len), _stream_ptr(stream))
+    _check(st, "pa_attention_noalloc")
+    return out
