@@ -42,8 +42,20 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
+STAMP = os.path.join(BUILD_DIR, "flags.txt")
+
+
+def extra_flags() -> list:
+    """Extra nvcc flags from PA_NVCC_EXTRA (e.g. tuning macros); recorded in a
+    stamp so a change of flags triggers a rebuild."""
+    return os.environ.get("PA_NVCC_EXTRA", "").split()
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB_PATH):
+        return False
+    stamp = open(STAMP).read() if os.path.exists(STAMP) else ""
+    if stamp != " ".join(extra_flags()):
         return False
     t = os.path.getmtime(LIB_PATH)
     return all(os.path.getmtime(d) <= t for d in _deps())
@@ -51,7 +63,7 @@ def up_to_date() -> bool:
 
 def _compile(src: str, verbose_ptxas: bool) -> str:
     obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra_flags(), "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -75,6 +87,8 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(STAMP, "w") as f:
+        f.write(" ".join(extra_flags()))
     return LIB_PATH
 
 

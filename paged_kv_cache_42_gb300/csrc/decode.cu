@@ -142,7 +142,7 @@ struct Cfg {
   static constexpr int KV_BYTES = kBlockSize * D * 2;
   static constexpr int Q_BYTES = G * D * 2;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
-  static constexpr int P_BYTES = kBlockSize * G * 4 + 64;  // p[16][G] then alpha[G]
+  static constexpr int P_BYTES = kBlockSize * G * 8 + 64;  // p[16][G] as {p,p} pairs, alpha[G]
   static_assert(TPT >= G, "a token's lane group must hold one value per head");
   static_assert(DPT == 8 || DPT == 16, "one or two 16-byte chunks per lane");
 };
@@ -210,10 +210,11 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   using WS = WarpSmem<D, G, NSTAGE>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t stage0 = smem_u32(smem + warp * WS::BYTES);
-  const uint32_t p_s = stage0 + NSTAGE * C::STAGE_BYTES;
-  const uint32_t alpha_s = p_s + kBlockSize * G * 4;
-  const uint32_t bars = p_s + C::P_BYTES;
+  unsigned char* const wsm = smem + warp * WS::BYTES;  // this warp's region
+  const uint32_t stage0 = smem_u32(wsm);
+  float2* const p_s = reinterpret_cast<float2*>(wsm + NSTAGE * C::STAGE_BYTES);  // [16][G]
+  float* const alpha_s = reinterpret_cast<float*>(p_s + kBlockSize * G);
+  const uint32_t bars = stage0 + NSTAGE * C::STAGE_BYTES + C::P_BYTES;
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < NSTAGE; ++s) mbar_init(bars + 8 * s, 1);
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     const int nb = __shfl_sync(kFull, cur.nb, j);
     const bool seg_start = (y == S) || blk == 0;
     const bool seg_end = (y == E - 1) || blk == nb - 1;
-    const uint32_t st_base = stage0 + stage * C::STAGE_BYTES;
+    const unsigned char* const st_ptr = wsm + stage * C::STAGE_BYTES;
     const uint32_t bar = bars + 8 * stage;
 
     if (!mbar_wait_bounded(bar, phase)) {
@@ -390,17 +391,17 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     }
 
     if (seg_start) {
-      const uint32_t qbase = st_base + 2 * C::KV_BYTES;
+      const unsigned char* const qbase = st_ptr + 2 * C::KV_BYTES;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const uint32_t row = qbase + h * D * 2 + sub * C::DPT * 2;
-        const uint4 a = lds128(row + 16 * swz);
+        const unsigned char* const row = qbase + h * D * 2 + sub * C::DPT * 2;
+        const uint4 a = *reinterpret_cast<const uint4*>(row + 16 * swz);
         qv[h][0] = bf16x2_to_float2(a.x);
         qv[h][1] = bf16x2_to_float2(a.y);
         qv[h][2] = bf16x2_to_float2(a.z);
         qv[h][3] = bf16x2_to_float2(a.w);
         if constexpr (C::DPT == 16) {
-          const uint4 b = lds128(row + 16 * (1 - swz));
+          const uint4 b = *reinterpret_cast<const uint4*>(row + 16 * (1 - swz));
           qv[h][4] = bf16x2_to_float2(b.x);
           qv[h][5] = bf16x2_to_float2(b.y);
           qv[h][6] = bf16x2_to_float2(b.z);
@@ -423,16 +424,16 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 #pragma unroll
     for (int ps = 0; ps < C::NPASS; ++ps) {
       const int t = ps * C::TPP + tg;
-      const uint32_t row = st_base + t * D * 2 + sub * C::DPT * 2;
+      const unsigned char* const row = st_ptr + t * D * 2 + sub * C::DPT * 2;
       float2 kf[C::DPT / 2];
       {
-        const uint4 a = lds128(row + 16 * swz);
+        const uint4 a = *reinterpret_cast<const uint4*>(row + 16 * swz);
         kf[0] = bf16x2_to_float2(a.x);
         kf[1] = bf16x2_to_float2(a.y);
         kf[2] = bf16x2_to_float2(a.z);
         kf[3] = bf16x2_to_float2(a.w);
         if constexpr (C::DPT == 16) {
-          const uint4 b = lds128(row + 16 * (1 - swz));
+          const uint4 b = *reinterpret_cast<const uint4*>(row + 16 * (1 - swz));
           kf[4] = bf16x2_to_float2(b.x);
           kf[5] = bf16x2_to_float2(b.y);
           kf[6] = bf16x2_to_float2(b.z);
@@ -447,8 +448,12 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
         for (int i = 1; i < C::DPT / 2; ++i) a2 = ffma2(qv[h][i], kf[i], a2);
         part[h] = a2.x + a2.y;
       }
-      const float s = reduce_heads<G, C::TPT>(part, lane);
-      sc[ps] = (t < nvalid) ? s : -INFINITY;
+      sc[ps] = reduce_heads<G, C::TPT>(part, lane);
+    }
+    if (nvalid < kBlockSize) {  // keys past the sequence end (their slots may hold anything)
+#pragma unroll
+      for (int ps = 0; ps < C::NPASS; ++ps)
+        if (ps * C::TPP + tg >= nvalid) sc[ps] = -INFINITY;
     }
 
     // ---- online softmax (base 2) ------------------------------------------------------
@@ -464,53 +469,53 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     for (int ps = 0; ps < C::NPASS; ++ps) {
       const float pr = exp2f(sc[ps] - m_new);
       psum += pr;
-      const int t = ps * C::TPP + tg;
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(p_s + (t * G + hsel) * 4), "f"(pr) : "memory");
+      p_s[(ps * C::TPP + tg) * G + hsel] = make_float2(pr, pr);
     }
     l_run = l_run * alpha + psum;
     m_run = m_new;
-    if (lane < G)
-      asm volatile("st.shared.f32 [%0], %1;" ::"r"(alpha_s + hsel * 4), "f"(alpha) : "memory");
+    // The accumulators need rescaling only when some head's running max moved
+    // (and not at all right after a segment start, when they are zero).
+    const bool rescale = !seg_start && !__all_sync(kFull, alpha == 1.f);
+    if (rescale && lane < G) alpha_s[hsel] = alpha;
     __syncwarp();
 
     // ---- o = o * alpha + sum_t p_t v_t ---------------------------------------------------
     {
-      float al[G];
+      if (rescale) {
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(al[h]) : "r"(alpha_s + h * 4));
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        acc[h][0] = fmul2(acc[h][0], make_float2(al[h], al[h]));
-        acc[h][1] = fmul2(acc[h][1], make_float2(al[h], al[h]));
+        for (int h = 0; h < G; ++h) {
+          const float al = alpha_s[h];
+          acc[h][0] = fmul2(acc[h][0], make_float2(al, al));
+          acc[h][1] = fmul2(acc[h][1], make_float2(al, al));
+        }
       }
+      // Keys past the sequence end have p = 0; their V rows (which may hold
+      // anything, NaN included) are replaced by the last valid row so the
+      // loop needs no per-token branch: 0 * finite adds nothing.
+      const unsigned char* const vbase = st_ptr + C::KV_BYTES + rl * 8;
+      const int tmax = nvalid - 1;
 #pragma unroll
       for (int stp = 0; stp < kBlockSize / C::RPS; ++stp) {
         const int t = stp * C::RPS + rrow;
-        if (t < nvalid) {
-          const uint2 vv = lds64(st_base + C::KV_BYTES + t * D * 2 + rl * 8);
+        {
+          const uint2 vv = *reinterpret_cast<const uint2*>(vbase + min(t, tmax) * D * 2);
           const float2 v01 = bf16x2_to_float2(vv.x);
           const float2 v23 = bf16x2_to_float2(vv.y);
-          float pp[G];
-          if constexpr (G >= 4) {
+          float2 ph[G];
+          if constexpr (G >= 2) {
 #pragma unroll
-            for (int h4 = 0; h4 < G; h4 += 4) {
-              const uint4 q4 = lds128(p_s + (t * G + h4) * 4);
-              pp[h4 + 0] = __uint_as_float(q4.x);
-              pp[h4 + 1] = __uint_as_float(q4.y);
-              pp[h4 + 2] = __uint_as_float(q4.z);
-              pp[h4 + 3] = __uint_as_float(q4.w);
+            for (int h2 = 0; h2 < G; h2 += 2) {
+              const float4 q4 = *reinterpret_cast<const float4*>(p_s + t * G + h2);
+              ph[h2] = make_float2(q4.x, q4.y);
+              ph[h2 + 1] = make_float2(q4.z, q4.w);
             }
           } else {
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[h]) : "r"(p_s + (t * G + h) * 4));
+            ph[0] = p_s[t];
           }
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float2 ph = make_float2(pp[h], pp[h]);
-            acc[h][0] = ffma2(ph, v01, acc[h][0]);
-            acc[h][1] = ffma2(ph, v23, acc[h][1]);
+            acc[h][0] = ffma2(ph[h], v01, acc[h][0]);
+            acc[h][1] = ffma2(ph[h], v23, acc[h][1]);
           }
         }
       }
@@ -677,21 +682,46 @@ cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, cudaStream_t s) 
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+// Warps per CTA and ring stages per warp. Each warp owns its ring, so these
+// set how many (block, kv head) tiles are in flight per SM and how many warps
+// hide each other's latency; shared memory per SM is the budget they share.
+#ifndef PA_DEC128_WARPS
+#define PA_DEC128_WARPS 4
+#endif
+#ifndef PA_DEC128_STAGES
+#define PA_DEC128_STAGES 2
+#endif
+#ifndef PA_DEC128G8_WARPS
+#define PA_DEC128G8_WARPS 4
+#endif
+#ifndef PA_DEC128G8_STAGES
+#define PA_DEC128G8_STAGES 2
+#endif
+#ifndef PA_DEC64_WARPS
+#define PA_DEC64_WARPS 4
+#endif
+#ifndef PA_DEC64_STAGES
+#define PA_DEC64_STAGES 3
+#endif
+
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
                           cudaStream_t s) {
+  constexpr int W128 = PA_DEC128_WARPS, S128 = PA_DEC128_STAGES;
+  constexpr int W128G8 = PA_DEC128G8_WARPS, S128G8 = PA_DEC128G8_STAGES;
+  constexpr int W64 = PA_DEC64_WARPS, S64 = PA_DEC64_STAGES;
   if (head_dim == 128) {
     switch (group) {
-      case 1: return launch_decode_t<128, 1, 4, 3>(p, num_sms, s);
-      case 2: return launch_decode_t<128, 2, 4, 3>(p, num_sms, s);
-      case 4: return launch_decode_t<128, 4, 4, 3>(p, num_sms, s);
-      case 8: return launch_decode_t<128, 8, 3, 3>(p, num_sms, s);
+      case 1: return launch_decode_t<128, 1, W128, S128>(p, num_sms, s);
+      case 2: return launch_decode_t<128, 2, W128, S128>(p, num_sms, s);
+      case 4: return launch_decode_t<128, 4, W128, S128>(p, num_sms, s);
+      case 8: return launch_decode_t<128, 8, W128G8, S128G8>(p, num_sms, s);
     }
   } else if (head_dim == 64) {
     switch (group) {
-      case 1: return launch_decode_t<64, 1, 4, 4>(p, num_sms, s);
-      case 2: return launch_decode_t<64, 2, 4, 4>(p, num_sms, s);
-      case 4: return launch_decode_t<64, 4, 4, 4>(p, num_sms, s);
-      case 8: return launch_decode_t<64, 8, 4, 4>(p, num_sms, s);
+      case 1: return launch_decode_t<64, 1, W64, S64>(p, num_sms, s);
+      case 2: return launch_decode_t<64, 2, W64, S64>(p, num_sms, s);
+      case 4: return launch_decode_t<64, 4, W64, S64>(p, num_sms, s);
+      case 8: return launch_decode_t<64, 8, W64, S64>(p, num_sms, s);
     }
   }
   return cudaErrorInvalidValue;
