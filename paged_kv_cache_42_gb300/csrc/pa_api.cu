@@ -135,7 +135,7 @@ size_t pa_attention_workspace_size(int num_reqs, int num_tokens, int num_q_heads
   if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       head_dim <= 0 || num_q_heads % num_kv_heads != 0)
     return 0;
-  return ws_layout(num_tokens, num_q_heads, num_kv_heads, head_dim).total;
+  return ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim).total;
 }
 
 pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
@@ -166,7 +166,7 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
   const long long max_blocks = ((long long)max_seq_len + kBlockSize - 1) / kBlockSize;
   if ((long long)num_tokens * num_kv_heads * max_blocks >= (1LL << 31))
     return PA_ERR_UNSUPPORTED;
-  const WsLayout lay = ws_layout(num_tokens, num_q_heads, num_kv_heads, head_dim);
+  const WsLayout lay = ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim);
   if (!workspace || workspace_bytes < lay.total ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PA_ERR_WORKSPACE;
@@ -185,13 +185,41 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
   pp.max_blocks_per_req = max_blocks_per_req;
   pp.max_query_len = max_query_len;
   pp.max_seq_len = max_seq_len;
+  pp.group = num_q_heads / num_kv_heads;
+  pp.use_prefill = max_query_len >= kPrefillMinQlen ? 1 : 0;
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
   pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
   pp.counters = reinterpret_cast<int*>(ws + lay.counters_off);
+  pp.tiles = reinterpret_cast<PrefillTile*>(ws + lay.tiles_off);
   pp.err = d->err;
   {
     TimerScope timer(1, s);
     const cudaError_t e = launch_plan(pp, s);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+
+  if (pp.use_prefill) {
+    PrefillLaunch pl;
+    pl.q = q;
+    pl.k_cache = k_cache;
+    pl.v_cache = v_cache;
+    pl.qsl = query_start_loc;
+    pl.seq_lens = seq_lens;
+    pl.block_tables = block_tables;
+    pl.out = static_cast<uint16_t*>(out);
+    pl.header = pp.header;
+    pl.tiles = pp.tiles;
+    pl.num_tokens = num_tokens;
+    pl.num_q_heads = num_q_heads;
+    pl.num_kv_heads = num_kv_heads;
+    pl.head_dim = head_dim;
+    pl.num_blocks = num_blocks;
+    pl.bt_stride = max_blocks_per_req;
+    pl.scale_log2 = scale * 1.4426950408889634f;
+    pl.err = d->err;
+    TimerScope timer(3, s);
+    const cudaError_t e = launch_prefill(pl, d->num_sms, s);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }

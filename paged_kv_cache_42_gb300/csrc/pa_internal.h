@@ -27,30 +27,49 @@ struct UnitInfo {
 static_assert(sizeof(UnitInfo) == 16, "UnitInfo is loaded as one 16-byte vector");
 
 struct WsHeader {
-  int num_units;      // K: tokens with work
+  int num_units;      // K: tokens with work on the split-KV path
   int num_positions;  // W: sum over units of Hkv * ceil(len / 16)
-  int pad[62];
+  int num_tiles;      // prefill-chunk tiles for the tensor-core path
+  int pad[61];
 };
+
+// Requests with at least this many new tokens go to the tensor-core
+// prefill-chunk kernel; shorter ones (decodes, short verify spans) to the
+// split-KV kernel.
+#ifndef PA_PREFILL_MIN_QLEN
+#define PA_PREFILL_MIN_QLEN 16
+#endif
+constexpr int kPrefillMinQlen = PA_PREFILL_MIN_QLEN;
+
+// One prefill work item: two 128-row tiles of request `req`, kv head `kv`,
+// chunk tokens j0 .. j0 + 2*128/G - 1, attending to nkv 128-key tiles.
+struct PrefillTile {
+  int req, kv, j0, nkv;
+};
+static_assert(sizeof(PrefillTile) == 16, "tiles are 16 bytes");
 static_assert(sizeof(WsHeader) == 256, "header occupies the first 256 bytes");
 
 // Workspace carve-up, identical on host and device.
 struct WsLayout {
-  size_t header_off, units_off, counters_off, partials_off, total;
+  size_t header_off, units_off, counters_off, tiles_off, partials_off, total;
   int slot_floats;  // floats per partial-result slot
 };
 
 __host__ __device__ inline size_t pa_align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-__host__ __device__ inline WsLayout ws_layout(int num_tokens, int num_q_heads, int num_kv_heads,
-                                              int head_dim) {
+__host__ __device__ inline WsLayout ws_layout(int num_reqs, int num_tokens, int num_q_heads,
+                                              int num_kv_heads, int head_dim) {
   WsLayout l;
   const int G = num_q_heads / num_kv_heads;
   l.slot_floats = 16 + G * head_dim;  // [m x G][l x G] padded to 16 floats, then o[G][D]
   l.header_off = 0;
   l.units_off = pa_align256(sizeof(WsHeader));
   l.counters_off = l.units_off + pa_align256(sizeof(UnitInfo) * (size_t)(num_tokens + 1));
-  l.partials_off =
+  l.tiles_off =
       l.counters_off + pa_align256(sizeof(int) * (size_t)num_tokens * (size_t)num_kv_heads);
+  // a chunk of qlen tokens makes ceil(qlen / (128 / G)) <= qlen / 16 + 1 tiles per kv head
+  const size_t max_tiles = (size_t)num_kv_heads * ((size_t)num_tokens / 16 + (size_t)num_reqs + 1);
+  l.partials_off = l.tiles_off + pa_align256(sizeof(PrefillTile) * max_tiles);
   const size_t slots = (size_t)num_tokens * num_kv_heads + kMaxDecodeWorkers;
   l.total = l.partials_off + pa_align256(sizeof(float) * (size_t)l.slot_floats * slots);
   return l;
@@ -60,9 +79,27 @@ struct PlanParams {
   const int32_t* qsl;
   const int32_t* seq_lens;
   int num_reqs, num_tokens, num_kv_heads, max_blocks_per_req, max_query_len, max_seq_len;
+  int group;        // G = Hq / Hkv
+  int use_prefill;  // route requests with qlen >= kPrefillMinQlen to the tensor-core kernel
   WsHeader* header;
   UnitInfo* units;
   int* counters;
+  PrefillTile* tiles;
+  unsigned long long* err;
+};
+
+struct PrefillLaunch {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  uint16_t* out;
+  const WsHeader* header;
+  const PrefillTile* tiles;
+  int num_tokens, num_q_heads, num_kv_heads, head_dim, num_blocks, bt_stride;
+  float scale_log2;
   unsigned long long* err;
 };
 
@@ -106,5 +143,6 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 // instantiation; unsupported combinations return cudaErrorInvalidValue.
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
                           cudaStream_t s);
+cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s);
 
 }  // namespace pa

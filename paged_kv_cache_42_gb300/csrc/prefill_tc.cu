@@ -1,0 +1,551 @@
+// Prefill-chunk attention on the tensor cores (tcgen05 + TMEM + TMA).
+//
+// What is computed ("vLLM v1 Deep Dive: How LLM(...) and the Server Boot and
+// Generate", Part 3, "Aside - KV cache and prefix caching": a prefill query
+// attends causally over [its already-cached prefix blocks] + [its new
+// tokens]): for a request with ctx cached tokens and a chunk of qlen new
+// tokens, new token j attends to keys 0 .. ctx + j, K/V read through the
+// request's block table.
+//
+// Tiling (ours). A row tile is 128 query rows of one (request, kv head): the G
+// query heads of the kv head times 128/G consecutive chunk tokens, row
+// m = token * G + head - the GQA "Q block" packing ("vLLM: An Exhaustive
+// Technical Study for Kernel Engineers", 2.4, Triton unified attention), so a
+// row tile shares one K/V stream. A CTA work item is a PAIR of adjacent row
+// tiles (256 rows) over the same keys; keys come in tiles of 128 = eight
+// 16-key cache blocks, loaded once for both row tiles.
+//
+//   S_t = Q_t K^T   tcgen05.mma kind::f16, M=128 N=128, A=Q_t and B=K from
+//                   128B-swizzled shared memory, fp32 into TMEM.
+//   softmax         one thread per row (one TMEM lane): mask, scale, running
+//                   max, exp2; P_t rounded to bf16 and written back into TMEM
+//                   over the S_t it came from.
+//   O_t += P_t V    tcgen05.mma with A=P_t from TMEM, B=V (M/N-major) from
+//                   shared memory, O_t in TMEM.
+// The two row tiles ping-pong: while one warpgroup runs the softmax of its
+// tile, the tensor core runs the other tile's P*V and next S.
+//
+// The running max is only moved (and O rescaled through TMEM) when it grows
+// by more than 2^8; otherwise P is formed against the stale max, which keeps
+// every P <= 256 and the result exact up to rounding.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads (both Q tiles per work
+// item, K into a 3-stage ring released right after both S MMAs of a key tile,
+// V into a 2-stage ring released after both P*V), warp 1 allocates TMEM and
+// one thread issues the MMAs in order
+//   S0(0) S1(0) | PV0(i) S0(i+1) PV1(i) S1(i+1) | ...
+// and warps 2-5 / 6-9 (warpgroup t; warp w reads TMEM lanes 32*(w%4)..) run
+// the softmax and epilogue of row tile t. Every wait is bounded; a wait that
+// gives up sets the device error word and the CTA winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pa_internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr unsigned kAll = 0xffffffffu;
+
+template <int D, int G>
+struct PCfg {
+  static constexpr int TOK = 128 / G;         // chunk tokens per 128-row tile
+  static constexpr int NCH = D / 64;          // 64-element (128-byte) d chunks
+  static constexpr int CHUNK = 128 * 128;     // one [128 rows][128 B] operand chunk
+  static constexpr int Q_BYTES = NCH * CHUNK; // one row tile of Q
+  static constexpr int KV_BYTES = NCH * CHUNK;  // one 128-key tile of K or of V
+  static constexpr int KSTAGES = 3;
+  static constexpr int VSTAGES = 2;
+  static constexpr int OFF_Q = 0;  // two row tiles
+  static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_V = OFF_K + KSTAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VSTAGES * KV_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + 1 KB alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  // S_t (fp32, 128 columns) at 128*t; P_t (bf16 pairs, 64 columns) overwrites
+  // the first half of S_t; O_t at 256 + 128*t.
+  static constexpr uint32_t TM_S = 0;
+  static constexpr uint32_t TM_O = 256;
+};
+
+// barrier slots
+enum : int {
+  B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2 /* x3 */, B_K_EMPTY = 5 /* x3 */,
+  B_V_FULL = 8 /* x2 */, B_V_EMPTY = 10 /* x2 */, B_S_FULL = 12 /* x2: per row tile */,
+  B_P_FULL = 14 /* x2 */, B_PV_DONE = 16 /* x2 */, B_O_EMPTY = 18 /* x2 */, B_DRAIN = 20,
+  B_COUNT = 21
+};
+
+constexpr int kThreads = 320;
+
+}  // namespace
+
+struct PrefillParams {
+  CUtensorMap tm_q;  // q as [T][Hq][D], box {64, G, 128/G}, 128B swizzle
+  CUtensorMap tm_k;  // k_cache as [(blocks * Hkv * 16)][D], box {64, 16}
+  CUtensorMap tm_v;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* block_tables;
+  uint16_t* out;
+  const WsHeader* header;
+  const PrefillTile* tiles;
+  int bt_stride, num_q_heads, num_kv_heads, num_blocks;
+  float scale_log2;
+  unsigned long long* err;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using C = PCfg<D, G>;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // operand tiles need 1024-byte alignment
+  unsigned char* const gbase = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = base + C::OFF_BAR;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::OFF_BAR + 8 * B_COUNT);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i) {
+      // P_FULL and O_EMPTY are arrived at by the 128 threads of one warpgroup;
+      // every other slot once, by an expect_tx arrive or an MMA commit.
+      const bool by_threads = (i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_EMPTY ||
+                               i == B_O_EMPTY + 1);
+      mbar_init(bar0 + 8 * i, by_threads ? 128 : 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  griddep_wait();  // the work list comes from the preceding (planner) grid
+  const int ntiles = p.header->num_tiles;
+
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8 * i; };
+  auto wait = [&](int i, uint32_t parity) -> bool {
+    if (mbar_wait_bounded(BAR(i), parity)) return true;
+    report_error(p.err, PA_DEVERR_WAIT_TIMEOUT, 1000 + i);
+    return false;
+  };
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    // Block ids are fetched 32 at a time (four key tiles), one group ahead;
+    // lanes 0..7 each copy one 16-key block.
+    int g = 0, it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
+      const PrefillTile tl = p.tiles[t];
+      const int q0 = __ldg(p.qsl + tl.req);
+      const int L = __ldg(p.seq_lens + tl.req);
+      const int nb = (L + kBlockSize - 1) / kBlockSize;
+      const int32_t* const bt_row = p.block_tables + (size_t)tl.req * p.bt_stride;
+      auto load_group = [&](int grp) -> int {
+        const int b = grp * 32 + lane;
+        if (b >= nb) return -1;
+        const int pid = __ldg(bt_row + b);
+        if (pid < 0 || pid >= p.num_blocks) {
+          report_error(p.err, PA_DEVERR_BLOCK_ID, b);
+          return -1;
+        }
+        return pid;
+      };
+      int pid_cur = load_group(0);
+      int pid_nxt = tl.nkv > 4 ? load_group(1) : -1;
+      if (it > 0 && !wait(B_Q_EMPTY, (it - 1) & 1)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(BAR(B_Q_FULL), 2 * C::Q_BYTES);
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(base + C::OFF_Q + rt * C::Q_BYTES + c * C::CHUNK, &p.tm_q, c * 64,
+                        tl.kv * G, q0 + tl.j0 + rt * C::TOK, BAR(B_Q_FULL));
+      }
+      for (int i = 0; i < tl.nkv; ++i, ++g) {
+        if (i > 0 && (i & 3) == 0) {
+          pid_cur = pid_nxt;
+          pid_nxt = (i + 4 < tl.nkv) ? load_group((i >> 2) + 1) : -1;
+        }
+        const int ks = g % C::KSTAGES, vs = g % C::VSTAGES;
+        const int pid = __shfl_sync(kAll, pid_cur, ((i & 3) << 3) + (lane & 7));
+        const int nload = __popc(__ballot_sync(kAll, lane < 8 && pid >= 0));
+        const int row = (pid * p.num_kv_heads + tl.kv) * kBlockSize;
+        const bool mine = lane < 8 && pid >= 0;
+        if (g >= C::KSTAGES && !wait(B_K_EMPTY + ks, ((g / C::KSTAGES) - 1) & 1)) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(BAR(B_K_FULL + ks), nload * C::NCH * 2048);
+        __syncwarp();
+        if (mine) {
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_2d(base + C::OFF_K + ks * C::KV_BYTES + c * C::CHUNK + lane * 2048, &p.tm_k,
+                        c * 64, row, BAR(B_K_FULL + ks));
+        }
+        if (g >= C::VSTAGES && !wait(B_V_EMPTY + vs, ((g / C::VSTAGES) - 1) & 1)) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(BAR(B_V_FULL + vs), nload * C::NCH * 2048);
+        __syncwarp();
+        if (mine) {
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_2d(base + C::OFF_V + vs * C::KV_BYTES + c * C::CHUNK + lane * 2048, &p.tm_v,
+                        c * 64, row, BAR(B_V_FULL + vs));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+    int gk = 0;   // key tiles whose S MMAs were issued
+    int gv = 0;   // key tiles whose P*V MMAs were issued
+    int np[2] = {0, 0};  // P_t events consumed
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
+      const PrefillTile tl = p.tiles[t];
+      const int L = __ldg(p.seq_lens + tl.req);
+      if (!wait(B_Q_FULL, it & 1)) { ok = false; break; }
+
+      // S_rt(key tile of counter gk) for row tile rt
+      auto issue_s = [&](int rt, bool last_of_item) -> bool {
+        const int kst = gk % C::KSTAGES;
+        if (rt == 0 && !wait(B_K_FULL + kst, (gk / C::KSTAGES) & 1)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem + C::TM_S + 128 * rt;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const int c = ks / 4, kk = ks % 4;
+            const uint64_t a = smem_desc_sw128(
+                base + C::OFF_Q + rt * C::Q_BYTES + c * C::CHUNK + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(
+                base + C::OFF_K + kst * C::KV_BYTES + c * C::CHUNK + kk * 32, 16, 1024);
+            umma_bf16(d, a, bd, idesc_qk, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(BAR(B_S_FULL + rt));
+          if (rt == 1) {
+            umma_commit(BAR(B_K_EMPTY + kst));
+            if (last_of_item) umma_commit(BAR(B_Q_EMPTY));
+          }
+        }
+        __syncwarp();
+        if (rt == 1) ++gk;
+        return true;
+      };
+      // P_rt(key tile i) * V for row tile rt
+      auto issue_pv = [&](int rt, int i) -> bool {
+        const int vst = gv % C::VSTAGES;
+        if (!wait(B_P_FULL + rt, np[rt] & 1)) return false;
+        ++np[rt];
+        if (rt == 0) {
+          if (!wait(B_V_FULL + vst, (gv / C::VSTAGES) & 1)) return false;
+          const int kv0 = i * 128;
+          if (kv0 + 128 > L) {
+            // Rows of keys past the sequence end may hold anything (NaN too);
+            // their P is 0, but 0 * NaN would poison O, so clear them.
+            const int r0 = L - kv0;
+            const int per_chunk = (128 - r0) * 8;  // 16-byte units
+            for (int idx = lane; idx < per_chunk * C::NCH; idx += 32) {
+              const int c = idx / per_chunk, rem = idx - c * per_chunk;
+              const int row = r0 + (rem >> 3), u = rem & 7;
+              *reinterpret_cast<uint4*>(gbase + C::OFF_V + vst * C::KV_BYTES + c * C::CHUNK +
+                                        row * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (i == 0 && it > 0 && !wait(B_O_EMPTY + rt, (it - 1) & 1)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t d = tmem + C::TM_O + 128 * rt;
+          const uint32_t a_tm = tmem + C::TM_S + 128 * rt;  // P_rt: 64 columns of bf16 pairs
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t bd =
+                smem_desc_sw128(base + C::OFF_V + vst * C::KV_BYTES + ks * 2048, C::CHUNK, 1024);
+            umma_bf16_ta(d, a_tm + 8 * ks, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(BAR(B_PV_DONE + rt));
+          if (rt == 1) umma_commit(BAR(B_V_EMPTY + vst));
+        }
+        __syncwarp();
+        if (rt == 1) ++gv;
+        return true;
+      };
+
+      ok = issue_s(0, tl.nkv == 1) && issue_s(1, tl.nkv == 1);
+      for (int i = 0; ok && i < tl.nkv; ++i) {
+        const bool more = i + 1 < tl.nkv;
+        const bool last_next = i + 2 == tl.nkv;
+        ok = issue_pv(0, i);
+        if (ok && more) ok = issue_s(0, last_next);
+        if (ok) ok = issue_pv(1, i);
+        if (ok && more) ok = issue_s(1, last_next);
+      }
+    }
+    // every MMA issued above has completed before TMEM is released
+    if (lane == 0) umma_commit(BAR(B_DRAIN));
+    __syncwarp();
+    mbar_wait_bounded(BAR(B_DRAIN), 0);
+  } else {
+    // ======================= softmax + epilogue (warpgroup rt: warps 2-5, 6-9) ==========
+    const int rt = (warp - 2) >> 2;  // row tile of this warpgroup
+    const int q4 = warp & 3;         // TMEM lane quarter this warp may access
+    const int m = q4 * 32 + lane;    // row == TMEM lane
+    const uint32_t trow = ((uint32_t)(q4 * 32) << 16) + tmem;
+    const uint32_t s_addr = trow + C::TM_S + 128 * rt;
+    const uint32_t o_addr = trow + C::TM_O + 128 * rt;
+    int ns = 0, it = 0;  // S_rt events consumed; work items done
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
+      const PrefillTile tl = p.tiles[t];
+      const int q0 = __ldg(p.qsl + tl.req);
+      const int qlen = __ldg(p.qsl + tl.req + 1) - q0;
+      const int L = __ldg(p.seq_lens + tl.req);
+      const int ctx = L - qlen;
+      const int j = tl.j0 + rt * C::TOK + m / G;  // chunk token of this row
+      const int lim = min(ctx + j, L - 1);         // last key this row may see
+      float m_used = -INFINITY, l = 0.f;
+      for (int i = 0; i < tl.nkv; ++i) {
+        // S_rt(i) complete implies every earlier MMA is too: O_rt is stable
+        // and P_rt(i-1) has been consumed.
+        if (!wait(B_S_FULL + rt, ns & 1)) { ok = false; break; }
+        ++ns;
+        tc_fence_after();
+        const int kv0 = i * 128;
+        const bool unmasked = __all_sync(kAll, kv0 + 127 <= lim);
+        // pass 1: row max of the raw scores over visible keys
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_addr + c * 32, r);
+          tmem_wait_ld();
+          if (unmasked) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[e]));
+          } else {
+            const int lim_c = lim - kv0 - c * 32;  // columns e <= lim_c are visible
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, e <= lim_c ? __uint_as_float(r[e]) : -INFINITY);
+          }
+        }
+        const float mt = mx * p.scale_log2;  // -inf stays -inf
+        float alpha = 1.f;
+        bool resc = false;
+        if (i == 0) {
+          m_used = mt;  // key 0 is always visible: finite
+        } else if (mt > m_used + 8.f) {
+          alpha = exp2f(m_used - mt);
+          m_used = mt;
+          resc = true;
+        }
+        if (__any_sync(kAll, resc)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_addr + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(o_addr + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        l *= alpha;
+        // pass 2: P = exp2(s * scale - m) as bf16 pairs, written over S: the 32
+        // S columns of chunk c become P columns 16c .. 16c+15, which only
+        // cover S columns already read.
+        const float nm = -m_used;
+        const float sc = p.scale_log2;
+        float l2[2] = {0.f, 0.f};  // two partial sums: shorter dependency chains
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(s_addr + c * 32, r);
+          tmem_wait_ld();
+          uint32_t w[16];
+          if (unmasked) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * e]), sc, nm));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), sc, nm));
+              l2[e & 1] += p0 + p1;
+              w[e] = float2_to_bf16x2(p0, p1);
+            }
+          } else {
+            const int lim_c = lim - kv0 - c * 32;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = 2 * e <= lim_c ? ex2_approx(fmaf(__uint_as_float(r[2 * e]), sc, nm)) : 0.f;
+              const float p1 =
+                  2 * e + 1 <= lim_c ? ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), sc, nm)) : 0.f;
+              l2[e & 1] += p0 + p1;
+              w[e] = float2_to_bf16x2(p0, p1);
+            }
+          }
+          tmem_st16(s_addr + 16 * c, w);
+        }
+        l += l2[0] + l2[1];
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(B_P_FULL + rt));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> bf16 rows of out ----
+      if (!wait(B_PV_DONE + rt, (ns - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool store = j < qlen;
+      uint16_t* const orow =
+          p.out + ((size_t)(q0 + j) * p.num_q_heads + (size_t)tl.kv * G + (m % G)) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_addr + c * 32, o);
+        tmem_wait_ld();
+        if (store) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 pk;
+            pk.x = float2_to_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            pk.y = float2_to_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            pk.z = float2_to_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            pk.w = float2_to_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * v) = pk;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(B_O_EMPTY + rt));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool encode_bf16(CUtensorMap* m, int rank, const void* ptr, const cuuint64_t* dims,
+                 const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr),
+                              dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
+  using C = PCfg<D, G>;
+  PrefillParams p;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
+    const cuuint64_t str[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.num_q_heads * D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)C::TOK};
+    if (!encode_bf16(&p.tm_q, 3, a.q, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t rows = (cuuint64_t)a.num_blocks * a.num_kv_heads * kBlockSize;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+    const cuuint64_t str[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+    if (!encode_bf16(&p.tm_k, 2, a.k_cache, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_bf16(&p.tm_v, 2, a.v_cache, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  p.qsl = a.qsl;
+  p.seq_lens = a.seq_lens;
+  p.block_tables = a.block_tables;
+  p.out = a.out;
+  p.header = a.header;
+  p.tiles = a.tiles;
+  p.bt_stride = a.bt_stride;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.num_blocks = a.num_blocks;
+  p.scale_log2 = a.scale_log2;
+  p.err = a.err;
+
+  auto kern = pa_prefill_kernel<D, G>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
+  if (!get_encoder()) return cudaErrorNotSupported;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  if (a.head_dim == 128) {
+    switch (G) {
+      case 1: return launch_prefill_t<128, 1>(a, num_sms, s);
+      case 2: return launch_prefill_t<128, 2>(a, num_sms, s);
+      case 4: return launch_prefill_t<128, 4>(a, num_sms, s);
+      case 8: return launch_prefill_t<128, 8>(a, num_sms, s);
+    }
+  } else if (a.head_dim == 64) {
+    switch (G) {
+      case 1: return launch_prefill_t<64, 1>(a, num_sms, s);
+      case 2: return launch_prefill_t<64, 2>(a, num_sms, s);
+      case 4: return launch_prefill_t<64, 4>(a, num_sms, s);
+      case 8: return launch_prefill_t<64, 8>(a, num_sms, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa
