@@ -263,7 +263,10 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
           for _ in range(steps)]
     dk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
-    for a, b in dk:  # materialise the event handles before handing them to the library
+    pk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    has_prefill = res.w.max_query_len >= 16
+    for a, b in dk + pk:  # materialise the event handles before handing them to the library
         a.record()
         b.record()
     torch.cuda.synchronize()
@@ -277,18 +280,23 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
     for i in range(steps):
         flush()
         binding.set_kernel_timer("decode", dk[i][0], dk[i][1])
+        if has_prefill:
+            binding.set_kernel_timer("prefill", pk[i][0], pk[i][1])
         ev[i][0].record(stream)
         fn()
         ev[i][1].record(stream)
     binding.set_kernel_timer("decode", None, None)
+    binding.set_kernel_timer("prefill", None, None)
     launches = binding.launch_count() - n0
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
     barrier(dist)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     dec_ms = [a.elapsed_time(b) for a, b in dk]
+    pre_ms = [a.elapsed_time(b) for a, b in pk] if has_prefill else [0.0]
     return {"ms_per_step": sum(step_ms) / steps, "ms_median": statistics.median(step_ms),
-            "decode_ms": sum(dec_ms) / steps, "launches": launches, "clocks": clk}
+            "decode_ms": sum(dec_ms) / steps, "prefill_ms": sum(pre_ms) / len(pre_ms),
+            "launches": launches, "clocks": clk}
 
 
 def run_ours(args, rank, world, local, dist):
@@ -328,8 +336,9 @@ def run_ours(args, rank, world, local, dist):
             raise RuntimeError(f"device error {code} at {detail}")
         ms = max_over_ranks(t["ms_per_step"], dist)
         dec_ms = max_over_ranks(t["decode_ms"], dist)
-        entry = {"w": w, "sb": sb, "t": t, "ms": ms, "dec_ms": dec_ms, "res": res,
-                 "steps": steps}
+        pre_ms = max_over_ranks(t["prefill_ms"], dist)
+        entry = {"w": w, "sb": sb, "t": t, "ms": ms, "dec_ms": dec_ms, "pre_ms": pre_ms,
+                 "res": res, "steps": steps}
         if idx == args.config and not args.no_e2e:
             te = time_steps(res, max(20, steps // 4), args.warmup, flush, torch, binding, dist,
                             e2e=True)
@@ -371,6 +380,7 @@ def run_ours(args, rank, world, local, dist):
             "algorithmic_bytes_per_launch": sb["attention"],
             "kernel_ms": round(main["dec_ms"], 5)},
         "gpu_launches": int(main["t"]["launches"]),
+        "prefill_kernel_ms": round(main["pre_ms"], 5) if main["pre_ms"] > 0 else None,
         "clocks": main["t"]["clocks"],
     }
     if w.shared_prefix_blocks:
@@ -389,6 +399,9 @@ def run_ours(args, rank, world, local, dist):
             "value": round(world * mw.num_tokens / (m["ms"] * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(m["ms"], 5), "steps": m["steps"],
             "attention_kernel_ms": round(m["dec_ms"], 5),
+            "prefill_kernel_ms": round(m["pre_ms"], 5),
+            "prefill_tflops": round(prefill_flops(mw) / (m["pre_ms"] * 1e-3) / 1e12, 1)
+            if m["pre_ms"] > 0 else None,
             "kv_bytes": m["sb"]["kv"], "prefill_causal_flops": prefill_flops(mw)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

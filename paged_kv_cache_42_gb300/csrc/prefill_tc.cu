@@ -207,6 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
     // ======================= MMA issuer =======================
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+    // Shared-memory descriptors differ only in their start address field
+    // (address >> 4), so each MMA takes a base descriptor plus a constant.
+    const uint64_t kmaj_base = smem_desc_sw128(base, 16, 1024);        // K-major (Q, K)
+    const uint64_t vmaj_base = smem_desc_sw128(base, C::CHUNK, 1024);  // M/N-major (V)
     int gk = 0;   // key tiles whose S MMAs were issued
     int gv = 0;   // key tiles whose P*V MMAs were issued
     int np[2] = {0, 0};  // P_t events consumed
@@ -224,14 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         tc_fence_after();
         if (lane == 0) {
           const uint32_t d = tmem + C::TM_S + 128 * rt;
+          const uint64_t a0 = kmaj_base + ((C::OFF_Q + rt * C::Q_BYTES) >> 4);
+          const uint64_t b0 = kmaj_base + ((C::OFF_K + kst * C::KV_BYTES) >> 4);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const int c = ks / 4, kk = ks % 4;
-            const uint64_t a = smem_desc_sw128(
-                base + C::OFF_Q + rt * C::Q_BYTES + c * C::CHUNK + kk * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(
-                base + C::OFF_K + kst * C::KV_BYTES + c * C::CHUNK + kk * 32, 16, 1024);
-            umma_bf16(d, a, bd, idesc_qk, ks > 0 ? 1u : 0u);
+            const int off = ((ks / 4) * C::CHUNK + (ks % 4) * 32) >> 4;
+            umma_bf16(d, a0 + off, b0 + off, idesc_qk, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(B_S_FULL + rt));
           if (rt == 1) {
@@ -271,12 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         if (lane == 0) {
           const uint32_t d = tmem + C::TM_O + 128 * rt;
           const uint32_t a_tm = tmem + C::TM_S + 128 * rt;  // P_rt: 64 columns of bf16 pairs
+          const uint64_t b0 = vmaj_base + ((C::OFF_V + vst * C::KV_BYTES) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t bd =
-                smem_desc_sw128(base + C::OFF_V + vst * C::KV_BYTES + ks * 2048, C::CHUNK, 1024);
-            umma_bf16_ta(d, a_tm + 8 * ks, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ta(d, a_tm + 8 * ks, b0 + ((ks * 2048) >> 4), idesc_pv,
+                         (i > 0 || ks > 0) ? 1u : 0u);
           umma_commit(BAR(B_PV_DONE + rt));
           if (rt == 1) umma_commit(BAR(B_V_EMPTY + vst));
         }
