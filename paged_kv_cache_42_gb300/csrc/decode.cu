@@ -143,9 +143,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   const int W = p.header->num_positions;
   const int K = p.header->num_units;
   if (W <= 0) return;
-  const int NW_all = gridDim.x * WARPS;
-  int NW = W / 8;  // at least 8 positions per worker
-  NW = NW < 1 ? 1 : (NW > NW_all ? NW_all : NW);
+  const int NW = plan_workers(W, gridDim.x * WARPS);
   const int w = blockIdx.x * WARPS + warp;
   if (w >= NW) return;
   const int S = (int)((long long)w * W / NW);
@@ -196,8 +194,13 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     return b;
   };
 
-  // ---- locate the first position: 32-ary search over units[].base --------------
+  // ---- the unit holding the first position: from the planner, or a 32-ary
+  // search over units[].base --------------------------------------------------------
   int lo = 0, hi = K;  // base[lo] <= S < base[hi]
+  if (p.worker_unit) {
+    lo = __ldg(p.worker_unit + w);
+    hi = lo + 1;
+  }
 #pragma unroll 1
   while (hi - lo > 1) {
     const int step = (hi - lo + 31) / 32;
@@ -566,8 +569,10 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 }
 
 // ---- launch ---------------------------------------------------------------------------
+// Grid of a split-KV launch on the current device: every SM filled to its
+// occupancy, capped so the workers fit the workspace's partial slots.
 template <int D, int G, int WARPS, int NSTAGE>
-cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, cudaStream_t s) {
+cudaError_t decode_grid(int num_sms, int* grid_out) {
   auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE>;
   constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE>::BYTES;
   static int occ_cache[64] = {0};
@@ -585,6 +590,17 @@ cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, cudaStream_t s) 
   }
   int grid = num_sms * occ;
   if (grid * WARPS > kMaxDecodeWorkers) grid = kMaxDecodeWorkers / WARPS;
+  *grid_out = grid;
+  return cudaSuccess;
+}
+
+template <int D, int G, int WARPS, int NSTAGE>
+cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, cudaStream_t s) {
+  auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE>;
+  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE>::BYTES;
+  int grid = 0;
+  cudaError_t e = decode_grid<D, G, WARPS, NSTAGE>(num_sms, &grid);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(WARPS * 32);
@@ -643,4 +659,31 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int nu
   return cudaErrorInvalidValue;
 }
 
+}  // namespace pa
+
+namespace pa {
+int decode_workers(int head_dim, int group, int num_sms) {
+  int grid = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  constexpr int W128 = PA_DEC128_WARPS, S128 = PA_DEC128_STAGES;
+  constexpr int W128G8 = PA_DEC128G8_WARPS, S128G8 = PA_DEC128G8_STAGES;
+  constexpr int W64 = PA_DEC64_WARPS, S64 = PA_DEC64_STAGES;
+  int warps = 0;
+  if (head_dim == 128) {
+    switch (group) {
+      case 1: e = decode_grid<128, 1, W128, S128>(num_sms, &grid); warps = W128; break;
+      case 2: e = decode_grid<128, 2, W128, S128>(num_sms, &grid); warps = W128; break;
+      case 4: e = decode_grid<128, 4, W128, S128>(num_sms, &grid); warps = W128; break;
+      case 8: e = decode_grid<128, 8, W128G8, S128G8>(num_sms, &grid); warps = W128G8; break;
+    }
+  } else if (head_dim == 64) {
+    switch (group) {
+      case 1: e = decode_grid<64, 1, W64, S64>(num_sms, &grid); warps = W64; break;
+      case 2: e = decode_grid<64, 2, W64, S64>(num_sms, &grid); warps = W64; break;
+      case 4: e = decode_grid<64, 4, W64, S64>(num_sms, &grid); warps = W64; break;
+      case 8: e = decode_grid<64, 8, W64, S64>(num_sms, &grid); warps = W64; break;
+    }
+  }
+  return e == cudaSuccess ? grid * warps : 0;
+}
 }  // namespace pa

@@ -187,10 +187,14 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
   pp.max_seq_len = max_seq_len;
   pp.group = num_q_heads / num_kv_heads;
   pp.use_prefill = max_query_len >= kPrefillMinQlen ? 1 : 0;
+  pp.num_workers = decode_workers(head_dim, pp.group, d->num_sms);
+  if (pp.num_workers <= 0) return PA_ERR_CUDA;
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
   pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
   pp.counters = reinterpret_cast<int*>(ws + lay.counters_off);
   pp.tiles = reinterpret_cast<PrefillTile*>(ws + lay.tiles_off);
+  pp.raw = reinterpret_cast<int2*>(ws + lay.raw_off);
+  pp.worker_unit = reinterpret_cast<int*>(ws + lay.workers_off);
   pp.err = d->err;
   {
     TimerScope timer(1, s);
@@ -237,6 +241,7 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
   dp.scale_log2 = scale * 1.4426950408889634f;
   dp.header = pp.header;
   dp.units = pp.units;
+  dp.worker_unit = num_tokens <= kPlanSmemTokens ? pp.worker_unit : nullptr;
   dp.counters = pp.counters;
   dp.partials = reinterpret_cast<float*>(ws + lay.partials_off);
   dp.slot_floats = lay.slot_floats;

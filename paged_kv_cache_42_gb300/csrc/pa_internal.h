@@ -14,6 +14,15 @@ constexpr int kBlockSize = 16;
 // The workspace reserves one partial-result slot per (token, kv head) plus one
 // per worker, so it is part of the workspace size formula.
 constexpr int kMaxDecodeWorkers = 4096;
+// The planner keeps per-token scratch in shared memory up to this many tokens.
+constexpr int kPlanSmemTokens = 4096;
+
+// Split-KV workers used for W flattened positions when `all` are launched:
+// at least 8 positions each (the planner and the split-KV kernel must agree).
+__host__ __device__ inline int plan_workers(int W, int all) {
+  int n = W / 8;
+  return n < 1 ? 1 : (n > all ? all : n);
+}
 
 // One entry per token that has keys to attend to, in token order (the
 // planner compacts away tokens with no work). `base` is the first position
@@ -51,7 +60,7 @@ static_assert(sizeof(WsHeader) == 256, "header occupies the first 256 bytes");
 
 // Workspace carve-up, identical on host and device.
 struct WsLayout {
-  size_t header_off, units_off, counters_off, tiles_off, partials_off, total;
+  size_t header_off, units_off, counters_off, tiles_off, raw_off, workers_off, partials_off, total;
   int slot_floats;  // floats per partial-result slot
 };
 
@@ -69,7 +78,9 @@ __host__ __device__ inline WsLayout ws_layout(int num_reqs, int num_tokens, int 
       l.counters_off + pa_align256(sizeof(int) * (size_t)num_tokens * (size_t)num_kv_heads);
   // a chunk of qlen tokens makes ceil(qlen / (128 / G)) <= qlen / 16 + 1 tiles per kv head
   const size_t max_tiles = (size_t)num_kv_heads * ((size_t)num_tokens / 16 + (size_t)num_reqs + 1);
-  l.partials_off = l.tiles_off + pa_align256(sizeof(PrefillTile) * max_tiles);
+  l.raw_off = l.tiles_off + pa_align256(sizeof(PrefillTile) * max_tiles);
+  l.workers_off = l.raw_off + pa_align256(8 * (size_t)num_tokens);
+  l.partials_off = l.workers_off + pa_align256(sizeof(int) * (size_t)kMaxDecodeWorkers);
   const size_t slots = (size_t)num_tokens * num_kv_heads + kMaxDecodeWorkers;
   l.total = l.partials_off + pa_align256(sizeof(float) * (size_t)l.slot_floats * slots);
   return l;
@@ -81,10 +92,13 @@ struct PlanParams {
   int num_reqs, num_tokens, num_kv_heads, max_blocks_per_req, max_query_len, max_seq_len;
   int group;        // G = Hq / Hkv
   int use_prefill;  // route requests with qlen >= kPrefillMinQlen to the tensor-core kernel
+  int num_workers;  // split-KV workers the decode launch provides
   WsHeader* header;
   UnitInfo* units;
   int* counters;
   PrefillTile* tiles;
+  int2* raw;        // per-token scratch when the batch is too large for shared memory
+  int* worker_unit; // first unit of each split-KV worker (only when the batch fits)
   unsigned long long* err;
 };
 
@@ -113,6 +127,7 @@ struct DecodeParams {
   float scale_log2;  // scale * log2(e): scores are kept in base-2 exponent units
   const WsHeader* header;
   const UnitInfo* units;
+  const int* worker_unit;  // null: each worker searches for its first unit
   int* counters;
   float* partials;
   int slot_floats;
@@ -143,6 +158,8 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 // instantiation; unsupported combinations return cudaErrorInvalidValue.
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
                           cudaStream_t s);
+// Split-KV workers launch_decode will use on this device (0 on error).
+int decode_workers(int head_dim, int group, int num_sms);
 cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s);
 
 }  // namespace pa

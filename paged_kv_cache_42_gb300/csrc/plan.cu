@@ -55,11 +55,18 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   __shared__ long long scan_sm[32];
   __shared__ int bucket_cnt[kTileBuckets];
   __shared__ int bucket_pos[kTileBuckets];
+  // Per-token scratch: {request, keys to attend}, then the compacted units'
+  // first positions. In shared memory when the batch fits, else in the
+  // workspace.
+  extern __shared__ int2 dsm[];
   const int T = p.num_tokens;
+  const bool in_smem = T <= kPlanSmemTokens;
+  int2* const raw = in_smem ? dsm : p.raw;
+  int* const ubase = in_smem ? reinterpret_cast<int*>(dsm + T) : nullptr;
   // a prefill work item is a pair of 128-row tiles: 2 * 128 / G chunk tokens
   const int tok_per_item = 2 * (128 / p.group);
   for (int b = threadIdx.x; b < kTileBuckets; b += blockDim.x) bucket_cnt[b] = 0;
-  for (int t = threadIdx.x; t < T; t += blockDim.x) p.units[t] = UnitInfo{t, -1, 0, 0};
+  for (int t = threadIdx.x; t < T; t += blockDim.x) raw[t] = make_int2(-1, 0);
   __syncthreads();
 
   // a request is valid when its span lies in [0, T] and its lengths agree
@@ -93,7 +100,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
         atomicAdd(&bucket_cnt[min(tile_nkv(L, ctx, j0), kTileBuckets - 1)], p.num_kv_heads);
       continue;  // these tokens are not on the split-KV path
     }
-    for (int j = 0; j < qlen; ++j) p.units[q0 + j] = UnitInfo{q0 + j, r, ctx + j + 1, 0};
+    for (int j = 0; j < qlen; ++j) raw[q0 + j] = make_int2(r, ctx + j + 1);
   }
   __syncthreads();
   {  // positions of the buckets, longest tiles first (exclusive scan, descending)
@@ -117,32 +124,82 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
       }
     }
   }
-  __syncthreads();
+  // compaction: tokens with keys become units with their first flattened position
   constexpr long long kLow = (1LL << 40) - 1;
   long long run_k = 0, run_w = 0;
   for (int c0 = 0; c0 < T; c0 += blockDim.x) {
     const int t = c0 + threadIdx.x;
-    const UnitInfo u = t < T ? p.units[t] : UnitInfo{0, -1, 0, 0};
-    const int nb = (u.len + kBlockSize - 1) / kBlockSize;
+    const int2 u = t < T ? raw[t] : make_int2(-1, 0);
+    const int nb = (u.y + kBlockSize - 1) / kBlockSize;
     const long long packed = ((long long)(nb > 0) << 40) | ((long long)nb * p.num_kv_heads);
     long long total;
-    const long long ex = block_exclusive_scan(packed, &total, scan_sm);
-    if (nb > 0) p.units[run_k + (ex >> 40)] = UnitInfo{u.tok, u.req, u.len, (int)(run_w + (ex & kLow))};
+    const long long ex = block_exclusive_scan(packed, &total, scan_sm);  // syncs: raw reads done
+    if (nb > 0) {
+      const int k = (int)(run_k + (ex >> 40));
+      const int base = (int)(run_w + (ex & kLow));
+      p.units[k] = UnitInfo{t, u.x, u.y, base};
+      if (ubase) ubase[k] = base;
+    }
     run_k += total >> 40;
     run_w += total & kLow;
   }
-  __syncthreads();
+  const int K = (int)run_k, W = (int)run_w;
   if (threadIdx.x == 0) {
-    p.units[run_k] = UnitInfo{T, -1, 0, (int)run_w};  // base[K] = W
-    p.header->num_units = (int)run_k;
-    p.header->num_positions = (int)run_w;
+    p.units[K] = UnitInfo{T, -1, 0, W};  // base[K] = W
+    if (ubase) ubase[K] = W;
+    p.header->num_units = K;
+    p.header->num_positions = W;
   }
   for (long long i = threadIdx.x; i < run_k * p.num_kv_heads; i += blockDim.x) p.counters[i] = 0;
+  // each split-KV worker's first unit (same worker count and slicing as the
+  // split-KV kernel), found by binary search over the units' first positions
+  if (ubase) {
+    __syncthreads();
+    const int NW = plan_workers(W, p.num_workers);
+    for (int w = threadIdx.x; w < NW; w += blockDim.x) {
+      const int S = (int)((long long)w * W / NW);
+      int lo = 0, hi = K;  // ubase[lo] <= S < ubase[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ubase[mid] <= S) lo = mid; else hi = mid;
+      }
+      p.worker_unit[w] = lo;
+    }
+  }
+  // Let the grid before this one (the KV write on the same stream) finish
+  // before this grid completes: whoever waits on the plan then also sees the
+  // newly written K/V.
+  griddep_wait();
 }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  pa_plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  const int smem = p.num_tokens <= kPlanSmemTokens
+                       ? (int)(sizeof(int2) * p.num_tokens + sizeof(int) * (p.num_tokens + 1))
+                       : 0;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(pa_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(int2) * kPlanSmemTokens + sizeof(int) * (kPlanSmemTokens + 1)));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  // Launched as a programmatic dependent of the previous grid (normally the
+  // KV write): it needs none of its output and overlaps it, and waits for it
+  // before completing.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa_plan_kernel, p);
 }
 
 }  // namespace pa

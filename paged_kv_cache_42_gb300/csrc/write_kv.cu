@@ -10,10 +10,14 @@
 // (D=128) or four (D=64) full rows with fully coalesced 128-bit loads and
 // stores. Bandwidth-bound, no shared memory.
 #include "pa_internal.h"
+#include "ptx.cuh"
 
 namespace pa {
 
 __global__ void __launch_bounds__(256) pa_write_kv_kernel(WriteParams p) {
+  // A planner launched next may start now: it reads only metadata, and
+  // waits for this grid before it completes.
+  griddep_launch_dependents();
   const int vec_per_row = p.head_dim / 8;  // 16-byte vectors per D-element row
   const long long total = (long long)p.num_tokens * p.num_kv_heads * vec_per_row;
   const uint4* k = reinterpret_cast<const uint4*>(p.k);

@@ -225,3 +225,15 @@ def test_inconsistent_lengths_are_reported():
     assert torch.isnan(out[1:].float()).all()  # rows of the bad request untouched
     ref = gu.oracle_reference(wl.subset_requests(w, [0]))
     gu.assert_close(gu.to_f64(out[:1]), ref, "good request next to a bad one")
+
+
+def test_batch_larger_than_planner_shared_memory():
+    # more than 4096 new tokens: the planner's scratch lives in the workspace
+    # and each split-KV worker searches for its first unit itself
+    rng = np.random.default_rng(11)
+    R = 4400
+    ctx = rng.integers(0, 300, size=R)
+    w = wl.make_workload(ctx, [1] * (R - 2) + [40, 17], num_q_heads=8, num_kv_heads=2,
+                         head_dim=64, seed=612, pool_factor=1.1)
+    assert w.num_tokens > 4096
+    _run_and_compare(w, "T > 4096", reqs=[0, 1, 2047, 4096, R - 3, R - 2, R - 1])
