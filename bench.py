@@ -405,7 +405,60 @@ def run_ours(args, rank, world, local, dist):
             "kv_bytes": m["sb"]["kv"], "prefill_causal_flops": prefill_flops(mw)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0 and not args.quick:
+        line["host_scheduler"] = host_scheduler_timing()
     return line
+
+
+def host_scheduler_timing(steps: int = 200) -> dict:
+    """Time the library's host scheduler step (pa_sched_step) forming the
+    mixed-batch shape: 512 decoding requests with the mixed workload's
+    context lengths plus 3 long prompts prefilled in 512-token chunks under
+    a 2048-token budget, prefix caching on. Only the C call is timed."""
+    from paged_kv_cache_42_gb300 import host
+
+    ctx, _, _ = wl.config_lengths(MIXED_CONFIG)
+    rng = np.random.Generator(np.random.PCG64(7))
+    pool = host.BlockPool(num_blocks=90000, block_size=16)
+    s = host.Scheduler(pool, token_budget=2048, max_model_len=4096, long_prefill_threshold=512,
+                       max_reqs=1024)
+    for i, c in enumerate(ctx[:512]):
+        s.add_request(i, rng.integers(0, 32000, int(c)))
+
+    def after(out):
+        nonlocal next_id
+        for rid in out["req_ids"]:
+            st = s.request_state(int(rid))
+            if st["num_computed"] == st["num_tokens"]:
+                if rid >= 512:
+                    s.finish(int(rid))
+                    s.add_request(next_id, rng.integers(0, 32000, 3500))
+                    next_id += 1
+                else:
+                    s.append_token(int(rid), int(rng.integers(0, 32000)))
+
+    next_id = 512
+    while True:  # bring all 512 requests to decoding
+        out = s.step()
+        after(out)
+        if s.num_waiting() == 0 and out["num_tokens"] == 512:
+            break
+    for _ in range(3):
+        s.add_request(next_id, rng.integers(0, 32000, 3500))
+        next_id += 1
+    times, shapes = [], set()
+    for _ in range(steps):
+        out = s.step()
+        times.append(s.last_step_seconds)
+        shapes.add((len(out["req_ids"]), out["num_tokens"]))
+        after(out)
+    t = np.asarray(times) * 1e6
+    return {"us_per_step_median": round(float(np.median(t)), 1),
+            "us_per_step_p90": round(float(np.percentile(t, 90)), 1), "steps": steps,
+            "batch": "512 decodes + 3 prefill chunks of 512, 2048 tokens",
+            "batch_shapes_seen": sorted(shapes)[:4],
+            "what": "pa_sched_step on one host core: budget pass, block allocation, prefix-cache "
+                    "registration (SHA-256), metadata arrays for the kernels"}
 
 
 # ---------------------------------------------------------------------------

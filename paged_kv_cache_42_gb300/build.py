@@ -1,7 +1,8 @@
 """Build ``libpagedattn.so`` in-tree with nvcc for sm_103a (GB300).
 
-Each ``csrc/*.cu`` file is compiled in parallel to an object, then linked into
-one shared library with the CUDA runtime linked statically, so the library
+Each ``csrc/*.cu`` file (kernels) is compiled with nvcc and each ``csrc/*.cpp``
+file (the host runtime: block pool, block hash, scheduler) with the host C++
+compiler, in parallel, then all objects are linked into one shared library with the CUDA runtime linked statically, so the library
 has no dependency beyond the driver. Run ``python -m
 paged_kv_cache_42_gb300.build`` or call :func:`build`.
 """
@@ -33,8 +34,15 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else (shutil.which("nvcc") or "nvcc")
 
 
+HOST_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-I", INCLUDE, "-I", CSRC]
+
+
+def cxx() -> str:
+    return os.environ.get("CXX") or shutil.which("g++") or "c++"
+
+
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -63,6 +71,12 @@ def up_to_date() -> bool:
 
 def _compile(src: str, verbose_ptxas: bool) -> str:
     obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+    if src.endswith(".cpp"):
+        cmd = [cxx(), *HOST_FLAGS, "-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"c++ failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra_flags(), "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
