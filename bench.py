@@ -48,6 +48,7 @@ from paged_kv_cache_42_gb300 import workloads as wl  # noqa: E402
 METRIC = "paged-attn decode KV GB/s (frac of HBM peak); mixed-batch tokens/s per layer"
 HEADLINE_CONFIG = 2
 MIXED_CONFIG = 3
+PREFIX_CONFIG = 4
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -210,10 +211,11 @@ class Resident:
     """A workload resident on the device plus the pinned host copies used by
     the end-to-end measurement."""
 
-    def __init__(self, w: wl.Workload, torch, binding):
+    def __init__(self, w: wl.Workload, torch, binding, cascade_len: int = 0):
         self.w = w
         self.torch = torch
         self.binding = binding
+        self.cascade_len = cascade_len  # > 0: attention through pa_attention_cascade
         dev = torch.device("cuda")
 
         def bf(bits):
@@ -232,18 +234,25 @@ class Resident:
         self.v_cache = bf(w.v_cache).to(dev)
         self.out = torch.empty_like(self.d["q"])
         self.h_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
-        self.ws = torch.empty(binding.workspace_size(w.num_reqs, w.num_tokens, w.num_q_heads,
-                                                     w.num_kv_heads, w.head_dim),
-                              dtype=torch.uint8, device=dev)
+        wsize = binding.cascade_workspace_size if cascade_len else binding.workspace_size
+        self.ws = torch.empty(wsize(w.num_reqs, w.num_tokens, w.num_q_heads, w.num_kv_heads,
+                                    w.head_dim), dtype=torch.uint8, device=dev)
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.h.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
 
     def step(self):
         d, w, b = self.d, self.w, self.binding
         b.write_kv(d["k"], d["v"], d["slot_mapping"], self.k_cache, self.v_cache)
-        b.attention(d["q"], self.k_cache, self.v_cache, d["block_tables"], d["seq_lens"],
-                    d["qsl"], w.scale, max_query_len=w.max_query_len,
-                    max_seq_len=w.max_seq_len, out=self.out, workspace=self.ws)
+        if self.cascade_len:
+            b.attention_cascade(d["q"], self.k_cache, self.v_cache, d["block_tables"],
+                                d["seq_lens"], d["qsl"], w.scale,
+                                common_prefix_len=self.cascade_len,
+                                max_query_len=w.max_query_len, max_seq_len=w.max_seq_len,
+                                out=self.out, workspace=self.ws)
+        else:
+            b.attention(d["q"], self.k_cache, self.v_cache, d["block_tables"], d["seq_lens"],
+                        d["qsl"], w.scale, max_query_len=w.max_query_len,
+                        max_seq_len=w.max_seq_len, out=self.out, workspace=self.ws)
 
     def step_e2e(self):
         for k, t in self.h.items():
@@ -265,7 +274,9 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
           for _ in range(steps)]
     pk = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
-    has_prefill = res.w.max_query_len >= 16
+    # the tensor-core kernel of the step: the cascade prefix pass, or prefill chunks
+    pre_kernel = "prefix" if res.cascade_len else "prefill"
+    has_prefill = bool(res.cascade_len) or res.w.max_query_len >= 16
     for a, b in dk + pk:  # materialise the event handles before handing them to the library
         a.record()
         b.record()
@@ -281,12 +292,12 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
         flush()
         binding.set_kernel_timer("decode", dk[i][0], dk[i][1])
         if has_prefill:
-            binding.set_kernel_timer("prefill", pk[i][0], pk[i][1])
+            binding.set_kernel_timer(pre_kernel, pk[i][0], pk[i][1])
         ev[i][0].record(stream)
         fn()
         ev[i][1].record(stream)
     binding.set_kernel_timer("decode", None, None)
-    binding.set_kernel_timer("prefill", None, None)
+    binding.set_kernel_timer(pre_kernel, None, None)
     launches = binding.launch_count() - n0
     torch.cuda.synchronize()
     clk = clocks.stop() if clocks else None
@@ -297,6 +308,39 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
     return {"ms_per_step": sum(step_ms) / steps, "ms_median": statistics.median(step_ms),
             "decode_ms": sum(dec_ms) / steps, "prefill_ms": sum(pre_ms) / len(pre_ms),
             "launches": launches, "clocks": clk}
+
+
+def prefix_share_timing(args, flush, torch, binding, dist, rank, world) -> dict:
+    """The prefix-sharing batch (every request shares one cached prefix),
+    stepped through pa_attention and through pa_attention_cascade."""
+    w = wl.make_config(PREFIX_CONFIG, seed=42 + PREFIX_CONFIG + 1000 * rank)
+    sb = step_bytes(w)
+    unique_attn = sb["attention"] - sb["kv"] + sb["kv_unique"]
+    steps = max(50, args.steps // 10)
+    out = {"workload": f"{wl.CONFIG_NAMES[PREFIX_CONFIG]}: "
+                       f"{wl.CONFIG_DESCRIPTIONS[PREFIX_CONFIG]}",
+           "steps": steps, "kv_bytes_logical": sb["kv"], "kv_bytes_unique": sb["kv_unique"]}
+    for name, casc in (("plain", 0), ("cascade", w.shared_prefix_blocks * 16)):
+        res = Resident(w, torch, binding, cascade_len=casc)
+        t = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
+        code, detail = binding.get_device_error(clear=True)
+        if code:
+            raise RuntimeError(f"device error {code} at {detail}")
+        ms = max_over_ranks(t["ms_per_step"], dist)
+        dec = max_over_ranks(t["decode_ms"], dist)
+        pre = max_over_ranks(t["prefill_ms"], dist) if casc else 0.0
+        attn_ms = dec + pre
+        out[name] = {"ms_per_step": round(ms, 5), "decode_kernel_ms": round(dec, 5),
+                     "tokens_per_s": round(world * w.num_tokens / (ms * 1e-3), 1),
+                     "attention_logical_gbs": round(sb["attention"] / (attn_ms * 1e-3) / 1e9, 1),
+                     "attention_unique_gbs": round(unique_attn / (attn_ms * 1e-3) / 1e9, 1)}
+        if casc:
+            out[name]["prefix_kernel_ms"] = round(pre, 5)
+            out[name]["common_prefix_len"] = casc
+        del res
+        torch.cuda.empty_cache()
+    out["cascade_speedup"] = round(out["plain"]["ms_per_step"] / out["cascade"]["ms_per_step"], 3)
+    return out
 
 
 def run_ours(args, rank, world, local, dist):
@@ -326,7 +370,8 @@ def run_ours(args, rank, world, local, dist):
     for idx in [args.config] + ([MIXED_CONFIG] if args.config != MIXED_CONFIG and not args.quick
                                 else []):
         w = wl.make_config(idx, seed=42 + idx + 1000 * rank)
-        res = Resident(w, torch, binding)
+        casc = w.shared_prefix_blocks * 16 if (args.cascade and idx == args.config) else 0
+        res = Resident(w, torch, binding, cascade_len=casc)
         sb = step_bytes(w)
         steps = args.steps if idx == args.config else max(50, args.steps // 10)
         t = time_steps(res, steps, args.warmup, flush, torch, binding, dist,
@@ -403,6 +448,8 @@ def run_ours(args, rank, world, local, dist):
             "prefill_tflops": round(prefill_flops(mw) / (m["pre_ms"] * 1e-3) / 1e12, 1)
             if m["pre_ms"] > 0 else None,
             "kv_bytes": m["sb"]["kv"], "prefill_causal_flops": prefill_flops(mw)}
+    if not args.quick and args.config != PREFIX_CONFIG:
+        line["prefix_share"] = prefix_share_timing(args, flush, torch, binding, dist, rank, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0 and not args.quick:
@@ -535,6 +582,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=HEADLINE_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--cascade", action="store_true",
+                    help="step the chosen workload through pa_attention_cascade (its shared "
+                         "prefix as the common prefix; the prefix-sharing workload has one)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

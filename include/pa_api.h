@@ -82,6 +82,8 @@ typedef enum pa_status {
 #define PA_DEVERR_LENGTHS 3      /* pa_attention: seq_len < query span, or too many blocks */
 #define PA_DEVERR_QSL 4          /* pa_attention: query_start_loc not within [0, num_tokens] */
 #define PA_DEVERR_WAIT_TIMEOUT 5 /* a kernel's bounded wait on a copy gave up */
+#define PA_DEVERR_PREFIX 6       /* pa_attention_cascade: a request's table does not start
+                                    with request 0's common-prefix blocks */
 
 /*
  * One-time per-device set-up for the current device (see the conventions).
@@ -153,6 +155,49 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        size_t workspace_bytes, void* stream);
 
 /*
+ * Cascade attention for a batch whose requests all share one common prefix
+ * ("vLLM: An Exhaustive Technical Study for Kernel Engineers", 2.3 Automatic
+ * prefix caching & KV reuse, cascade attention: when every request of a batch
+ * shares one prefix, attention over the prefix is computed once for the whole
+ * batch and merged with each request's attention over its own suffix by
+ * log-sum-exp renormalisation; metadata common_prefix_len).
+ *
+ * The result equals pa_attention's on the same arguments (up to fp32 rounding
+ * order). Arguments are pa_attention's plus:
+ *   common_prefix_len  tokens of the shared prefix: a positive multiple of
+ *                      block_size. Every request's first common_prefix_len /
+ *                      block_size block-table entries must equal request 0's,
+ *                      and every request's context (seq_len minus its new
+ *                      tokens) must be at least common_prefix_len, so that
+ *                      each new token sees the whole prefix.
+ *   workspace          at least pa_attention_cascade_workspace_size(...) bytes.
+ * The prefix pass runs on the tensor cores: for each KV head, the prefix keys
+ * against the queries of every new token of the batch (all G heads), split
+ * over key chunks, giving fp32 partials (max, sum, unnormalised output) in
+ * the workspace. The split-KV kernel then attends each token to its own
+ * suffix keys only and folds the prefix partials into its merge. Every span
+ * is handled by the split-KV kernel (no prefill-chunk tiles).
+ * Errors: host-side as pa_attention, plus PA_ERR_INVALID_ARG for a
+ * common_prefix_len that is not a positive multiple of block_size. On the
+ * device, a request whose context is shorter than the prefix sets
+ * PA_DEVERR_LENGTHS and is skipped (its rows untouched); a request whose
+ * table does not start with request 0's prefix blocks sets PA_DEVERR_PREFIX,
+ * and its rows are computed with request 0's prefix (they are wrong; the
+ * error word says so).
+ */
+size_t pa_attention_cascade_workspace_size(int num_reqs, int num_tokens, int num_q_heads,
+                                           int num_kv_heads, int head_dim);
+
+pa_status pa_attention_cascade(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, float scale, void* out,
+                               int num_reqs, int num_tokens, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_req, int max_query_len, int max_seq_len,
+                               int common_prefix_len, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
  * pa_attention without a caller-provided workspace, for callers that cannot
  * allocate device memory (for example code running inside an allocator's own
  * callbacks, or under a host framework that owns all device memory and offers
@@ -204,7 +249,7 @@ pa_status pa_get_device_error(int* code, long long* detail, int clear);
  * Instrumentation: record `start_event` / `stop_event` (cudaEvent_t handles
  * created by the caller) around every later launch of the given kernel on its
  * stream; pass NULL events to stop. Kernel ids: 0 write_kv, 1 planner,
- * 2 decode (split-KV), 3 prefill chunk. Process-wide setting, not thread-safe.
+ * 2 decode (split-KV), 3 prefill chunk, 4 cascade prefix pass. Process-wide setting, not thread-safe.
  */
 pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event);
 

@@ -27,8 +27,8 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED",
           -3: "PA_ERR_WORKSPACE", -4: "PA_ERR_CUDA", -5: "PA_ERR_BOUNDS", -6: "PA_ERR_TIMEOUT"}
 DEVICE_ERRORS = {0: "none", 1: "slot outside the pool", 2: "block id outside the pool",
                  3: "inconsistent lengths", 4: "query_start_loc out of range",
-                 5: "bounded wait timed out"}
-KERNEL_IDS = {"write_kv": 0, "plan": 1, "decode": 2, "prefill": 3}
+                 5: "bounded wait timed out", 6: "table does not start with the common prefix"}
+KERNEL_IDS = {"write_kv": 0, "plan": 1, "decode": 2, "prefill": 3, "prefix": 4}
 
 
 class PagedAttentionError(RuntimeError):
@@ -61,6 +61,12 @@ def lib() -> ctypes.CDLL:
                                    _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
                                    _c_p, ctypes.c_size_t, _c_p]
         L.pa_attention.restype = _c_i
+        L.pa_attention_cascade_workspace_size.argtypes = [_c_i, _c_i, _c_i, _c_i, _c_i]
+        L.pa_attention_cascade_workspace_size.restype = ctypes.c_size_t
+        L.pa_attention_cascade.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, ctypes.c_float,
+                                           _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
+                                           _c_i, _c_i, _c_i, _c_p, ctypes.c_size_t, _c_p]
+        L.pa_attention_cascade.restype = _c_i
         L.pa_status_string.argtypes = [_c_i]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_get_device_error.argtypes = [ctypes.POINTER(_c_i), ctypes.POINTER(ctypes.c_longlong),
@@ -161,6 +167,43 @@ def attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         int(max_query_len), int(max_seq_len), _dev(workspace, torch.uint8, "workspace"),
         int(workspace.numel()), _stream_ptr(stream))
     _check(st, "pa_attention")
+    return out
+
+
+def cascade_workspace_size(num_reqs: int, num_tokens: int, num_q_heads: int, num_kv_heads: int,
+                           head_dim: int) -> int:
+    return int(lib().pa_attention_cascade_workspace_size(num_reqs, num_tokens, num_q_heads,
+                                                         num_kv_heads, head_dim))
+
+
+def attention_cascade(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                      query_start_loc: torch.Tensor, scale: float, *, common_prefix_len: int,
+                      max_query_len: int, max_seq_len: int, out: torch.Tensor | None = None,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_attention_cascade: every request shares the first ``common_prefix_len``
+    keys (the same blocks); the prefix is attended once for the whole batch."""
+    T, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    R = int(seq_lens.shape[0])
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q and the caches")
+    if query_start_loc.shape != (R + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != R:
+        raise ValueError("metadata shapes must be qsl [R+1], block_tables [R, max_blocks]")
+    if out is None:
+        out = torch.empty_like(q)
+    need = cascade_workspace_size(R, T, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().pa_attention_cascade(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
+        _dev(seq_lens, torch.int32, "seq_lens"),
+        _dev(query_start_loc, torch.int32, "query_start_loc"), float(scale),
+        _dev(out, torch.bfloat16, "out"), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+        int(max_query_len), int(max_seq_len), int(common_prefix_len),
+        _dev(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream_ptr(stream))
+    _check(st, "pa_attention_cascade")
     return out
 
 

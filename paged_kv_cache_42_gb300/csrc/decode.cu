@@ -58,7 +58,7 @@ struct Cfg {
   static constexpr int KV_BYTES = kBlockSize * D * 2;
   static constexpr int Q_BYTES = G * D * 2;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
-  static constexpr int P_BYTES = kBlockSize * G * 8 + 64;  // p[16][G] as {p,p} pairs, alpha[G]
+  static constexpr int P_BYTES = kBlockSize * G * 4 + 64;  // p[16][G], alpha[G]
   static_assert(TPT >= G, "a token's lane group must hold one value per head");
   static_assert(DPT == 8 || DPT == 16, "one or two 16-byte chunks per lane");
 };
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* const wsm = smem + warp * WS::BYTES;  // this warp's region
   const uint32_t stage0 = smem_u32(wsm);
-  float2* const p_s = reinterpret_cast<float2*>(wsm + NSTAGE * C::STAGE_BYTES);  // [16][G]
+  float* const p_s = reinterpret_cast<float*>(wsm + NSTAGE * C::STAGE_BYTES);  // [16][G]
   float* const alpha_s = reinterpret_cast<float*>(p_s + kBlockSize * G);
   const uint32_t bars = stage0 + NSTAGE * C::STAGE_BYTES + C::P_BYTES;
   if (lane == 0) {
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   const int E = (int)((long long)(w + 1) * W / NW);
   if (S >= E) return;
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
+  const int kstart = p.key_start_blocks;  // first block on this path (cascade prefix skipped)
 
   auto worker_of = [&](int x) -> int { return (int)(((long long)(x + 1) * NW - 1) / W); };
 
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     b.tok = kl.tok;
     b.len = kl.len;
     const int base = kl.base;
-    int nb = (b.len + kBlockSize - 1) / kBlockSize;
+    int nb = (b.len + kBlockSize - 1) / kBlockSize - kstart;  // blocks after a cascade prefix
     nb = nb < 1 ? 1 : nb;
     b.nb = nb;
     b.end = base + nb * Hkv;
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     b.blk = off - b.kv * nb;
     int pid = 0;
     if (y < E) {
-      pid = __ldg(p.block_tables + (size_t)kl.req * p.bt_stride + b.blk);
+      pid = __ldg(p.block_tables + (size_t)kl.req * p.bt_stride + kstart + b.blk);
       if (pid < 0 || pid >= p.num_blocks) {
         report_error(p.err, PA_DEVERR_BLOCK_ID, y);
         pid = 0;
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
       l_run = 0.f;
     }
 
-    const int nvalid = min(kBlockSize, len - blk * kBlockSize);
+    const int nvalid = min(kBlockSize, len - (kstart + blk) * kBlockSize);
 
     // ---- scores: s = (q * scale * log2 e) . k for the lane's (head, token) ---------
     float sc[C::NPASS];
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     for (int ps = 0; ps < C::NPASS; ++ps) {
       const float pr = exp2f(sc[ps] - m_new);
       psum += pr;
-      p_s[(ps * C::TPP + tg) * G + hsel] = make_float2(pr, pr);
+      p_s[(ps * C::TPP + tg) * G + hsel] = pr;
     }
     l_run = l_run * alpha + psum;
     m_run = m_new;
@@ -421,15 +422,21 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
           const float2 v01 = bf16x2_to_float2(vv.x);
           const float2 v23 = bf16x2_to_float2(vv.y);
           float2 ph[G];
-          if constexpr (G >= 2) {
+          if constexpr (G >= 4) {
 #pragma unroll
-            for (int h2 = 0; h2 < G; h2 += 2) {
-              const float4 q4 = *reinterpret_cast<const float4*>(p_s + t * G + h2);
-              ph[h2] = make_float2(q4.x, q4.y);
-              ph[h2 + 1] = make_float2(q4.z, q4.w);
+            for (int h4 = 0; h4 < G; h4 += 4) {
+              const float4 q4 = *reinterpret_cast<const float4*>(p_s + t * G + h4);
+              ph[h4] = make_float2(q4.x, q4.x);
+              ph[h4 + 1] = make_float2(q4.y, q4.y);
+              ph[h4 + 2] = make_float2(q4.z, q4.z);
+              ph[h4 + 3] = make_float2(q4.w, q4.w);
             }
+          } else if constexpr (G == 2) {
+            const float2 q2 = *reinterpret_cast<const float2*>(p_s + t * 2);
+            ph[0] = make_float2(q2.x, q2.x);
+            ph[1] = make_float2(q2.y, q2.y);
           } else {
-            ph[0] = p_s[t];
+            ph[0] = make_float2(p_s[t], p_s[t]);
           }
 #pragma unroll
           for (int h = 0; h < G; ++h) {
@@ -490,8 +497,51 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
       const int ustart = y - blk;  // first position of this (token, kv head)
       const int wf = worker_of(ustart), wl = worker_of(ustart + nb - 1);
       uint16_t* orow = p.out + ((size_t)tok * Hq + (size_t)kv * G) * D + rl * 4;
+      // Cascade: the prefix partials of this (token, kv head), one per key
+      // chunk, folded into (M, Ls, O) by log-sum-exp renormalisation.
+      auto fold_prefix = [&](float (&M)[G], float (&Ls)[G], float4 (&O)[G]) {
+#pragma unroll 1
+        for (int c = 0; c < p.prefix_chunks; ++c) {
+          const float* sl =
+              p.prefix_partials + ((size_t)c * p.num_tokens + tok) * Hkv * p.slot_floats +
+              (size_t)kv * p.slot_floats;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float ms = __ldcg(sl + h);
+            const float mn = fmaxf(M[h], ms);
+            const float a = exp2f(M[h] - mn), b = exp2f(ms - mn);
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D + rl * 4));
+            Ls[h] = Ls[h] * a + __ldcg(sl + G + h) * b;
+            O[h].x = O[h].x * a + o.x * b;
+            O[h].y = O[h].y * a + o.y * b;
+            O[h].z = O[h].z * a + o.z * b;
+            O[h].w = O[h].w * a + o.w * b;
+            M[h] = mn;
+          }
+        }
+      };
       if (wf == wl) {
-        if (rrow == 0) {
+        if (p.prefix_partials) {
+          float M[G], Ls[G];
+          float4 O[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            M[h] = mh[h];
+            Ls[h] = lh[h];
+            O[h] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+          }
+          fold_prefix(M, Ls, O);
+          if (rrow == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float inv = 1.f / Ls[h];
+              uint2 pk;
+              pk.x = float2_to_bf16x2(O[h].x * inv, O[h].y * inv);
+              pk.y = float2_to_bf16x2(O[h].z * inv, O[h].w * inv);
+              *reinterpret_cast<uint2*>(orow + h * D) = pk;
+            }
+          }
+        } else if (rrow == 0) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             const float inv = 1.f / lh[h];
@@ -552,6 +602,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
               O[h].w += o.w * f;
             }
           }
+          if (p.prefix_partials) fold_prefix(M, Ls, O);
           if (rrow == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -572,7 +623,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 // Grid of a split-KV launch on the current device: every SM filled to its
 // occupancy, capped so the workers fit the workspace's partial slots.
 template <int D, int G, int WARPS, int NSTAGE>
-cudaError_t decode_grid(int num_sms, int* grid_out) {
+cudaError_t decode_grid(int num_sms, int occ_cap, int* grid_out) {
   auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE>;
   constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE>::BYTES;
   static int occ_cache[64] = {0};
@@ -588,6 +639,7 @@ cudaError_t decode_grid(int num_sms, int* grid_out) {
     if (occ < 1) occ = 1;
     if (dev >= 0 && dev < 64) occ_cache[dev] = occ;
   }
+  if (occ > occ_cap) occ = occ_cap;
   int grid = num_sms * occ;
   if (grid * WARPS > kMaxDecodeWorkers) grid = kMaxDecodeWorkers / WARPS;
   *grid_out = grid;
@@ -595,11 +647,11 @@ cudaError_t decode_grid(int num_sms, int* grid_out) {
 }
 
 template <int D, int G, int WARPS, int NSTAGE>
-cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, cudaStream_t s) {
+cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s) {
   auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE>;
   constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE>::BYTES;
   int grid = 0;
-  cudaError_t e = decode_grid<D, G, WARPS, NSTAGE>(num_sms, &grid);
+  cudaError_t e = decode_grid<D, G, WARPS, NSTAGE>(num_sms, occ_cap, &grid);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -637,23 +689,23 @@ cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, cudaStream_t s) 
 #endif
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
-                          cudaStream_t s) {
+                          int occ_cap, cudaStream_t s) {
   constexpr int W128 = PA_DEC128_WARPS, S128 = PA_DEC128_STAGES;
   constexpr int W128G8 = PA_DEC128G8_WARPS, S128G8 = PA_DEC128G8_STAGES;
   constexpr int W64 = PA_DEC64_WARPS, S64 = PA_DEC64_STAGES;
   if (head_dim == 128) {
     switch (group) {
-      case 1: return launch_decode_t<128, 1, W128, S128>(p, num_sms, s);
-      case 2: return launch_decode_t<128, 2, W128, S128>(p, num_sms, s);
-      case 4: return launch_decode_t<128, 4, W128, S128>(p, num_sms, s);
-      case 8: return launch_decode_t<128, 8, W128G8, S128G8>(p, num_sms, s);
+      case 1: return launch_decode_t<128, 1, W128, S128>(p, num_sms, occ_cap, s);
+      case 2: return launch_decode_t<128, 2, W128, S128>(p, num_sms, occ_cap, s);
+      case 4: return launch_decode_t<128, 4, W128, S128>(p, num_sms, occ_cap, s);
+      case 8: return launch_decode_t<128, 8, W128G8, S128G8>(p, num_sms, occ_cap, s);
     }
   } else if (head_dim == 64) {
     switch (group) {
-      case 1: return launch_decode_t<64, 1, W64, S64>(p, num_sms, s);
-      case 2: return launch_decode_t<64, 2, W64, S64>(p, num_sms, s);
-      case 4: return launch_decode_t<64, 4, W64, S64>(p, num_sms, s);
-      case 8: return launch_decode_t<64, 8, W64, S64>(p, num_sms, s);
+      case 1: return launch_decode_t<64, 1, W64, S64>(p, num_sms, occ_cap, s);
+      case 2: return launch_decode_t<64, 2, W64, S64>(p, num_sms, occ_cap, s);
+      case 4: return launch_decode_t<64, 4, W64, S64>(p, num_sms, occ_cap, s);
+      case 8: return launch_decode_t<64, 8, W64, S64>(p, num_sms, occ_cap, s);
     }
   }
   return cudaErrorInvalidValue;
@@ -662,7 +714,7 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int nu
 }  // namespace pa
 
 namespace pa {
-int decode_workers(int head_dim, int group, int num_sms) {
+int decode_workers(int head_dim, int group, int num_sms, int occ_cap) {
   int grid = 0;
   cudaError_t e = cudaErrorInvalidValue;
   constexpr int W128 = PA_DEC128_WARPS, S128 = PA_DEC128_STAGES;
@@ -671,17 +723,17 @@ int decode_workers(int head_dim, int group, int num_sms) {
   int warps = 0;
   if (head_dim == 128) {
     switch (group) {
-      case 1: e = decode_grid<128, 1, W128, S128>(num_sms, &grid); warps = W128; break;
-      case 2: e = decode_grid<128, 2, W128, S128>(num_sms, &grid); warps = W128; break;
-      case 4: e = decode_grid<128, 4, W128, S128>(num_sms, &grid); warps = W128; break;
-      case 8: e = decode_grid<128, 8, W128G8, S128G8>(num_sms, &grid); warps = W128G8; break;
+      case 1: e = decode_grid<128, 1, W128, S128>(num_sms, occ_cap, &grid); warps = W128; break;
+      case 2: e = decode_grid<128, 2, W128, S128>(num_sms, occ_cap, &grid); warps = W128; break;
+      case 4: e = decode_grid<128, 4, W128, S128>(num_sms, occ_cap, &grid); warps = W128; break;
+      case 8: e = decode_grid<128, 8, W128G8, S128G8>(num_sms, occ_cap, &grid); warps = W128G8; break;
     }
   } else if (head_dim == 64) {
     switch (group) {
-      case 1: e = decode_grid<64, 1, W64, S64>(num_sms, &grid); warps = W64; break;
-      case 2: e = decode_grid<64, 2, W64, S64>(num_sms, &grid); warps = W64; break;
-      case 4: e = decode_grid<64, 4, W64, S64>(num_sms, &grid); warps = W64; break;
-      case 8: e = decode_grid<64, 8, W64, S64>(num_sms, &grid); warps = W64; break;
+      case 1: e = decode_grid<64, 1, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
+      case 2: e = decode_grid<64, 2, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
+      case 4: e = decode_grid<64, 4, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
+      case 8: e = decode_grid<64, 8, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
     }
   }
   return e == cudaSuccess ? grid * warps : 0;

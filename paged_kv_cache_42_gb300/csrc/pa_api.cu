@@ -31,8 +31,9 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<long long> g_launches{0};
-cudaEvent_t g_timer_start[4] = {nullptr, nullptr, nullptr, nullptr};
-cudaEvent_t g_timer_stop[4] = {nullptr, nullptr, nullptr, nullptr};
+constexpr int kNumTimers = 5;  // write, plan, decode, prefill, cascade prefix
+cudaEvent_t g_timer_start[kNumTimers] = {};
+cudaEvent_t g_timer_stop[kNumTimers] = {};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -138,13 +139,26 @@ size_t pa_attention_workspace_size(int num_reqs, int num_tokens, int num_q_heads
   return ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim).total;
 }
 
-pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
-                       const int32_t* block_tables, const int32_t* seq_lens,
-                       const int32_t* query_start_loc, float scale, void* out, int num_reqs,
-                       int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
-                       int block_size, int num_blocks, int max_blocks_per_req,
-                       int max_query_len, int max_seq_len, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+size_t pa_attention_cascade_workspace_size(int num_reqs, int num_tokens, int num_q_heads,
+                                           int num_kv_heads, int head_dim) {
+  const size_t base =
+      pa_attention_workspace_size(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim);
+  if (base == 0) return 0;
+  return base + prefix_partials_bytes(num_tokens, num_q_heads, num_kv_heads, head_dim);
+}
+
+}  // extern "C"
+
+namespace {
+
+// pa_attention and pa_attention_cascade (prefix_len > 0).
+pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens,
+                         const int32_t* query_start_loc, float scale, void* out, int num_reqs,
+                         int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int num_blocks, int max_blocks_per_req,
+                         int max_query_len, int max_seq_len, int prefix_len, void* workspace,
+                         size_t workspace_bytes, void* stream) {
   if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       head_dim <= 0 || num_blocks < 0 || max_blocks_per_req < 0 || max_query_len < 0 ||
       max_seq_len < 0)
@@ -166,9 +180,16 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
   const long long max_blocks = ((long long)max_seq_len + kBlockSize - 1) / kBlockSize;
   if ((long long)num_tokens * num_kv_heads * max_blocks >= (1LL << 31))
     return PA_ERR_UNSUPPORTED;
+  // a cascade prefix is whole blocks, inside the tables, and leaves every
+  // request at least one key of its own
+  if (prefix_len > 0 && (prefix_len / kBlockSize > max_blocks_per_req || prefix_len >= max_seq_len))
+    return PA_ERR_INVALID_ARG;
   const WsLayout lay = ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim);
-  if (!workspace || workspace_bytes < lay.total ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+  const size_t need =
+      lay.total + (prefix_len > 0
+                       ? prefix_partials_bytes(num_tokens, num_q_heads, num_kv_heads, head_dim)
+                       : 0);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return PA_ERR_WORKSPACE;
 
   DeviceState* d = nullptr;
@@ -176,18 +197,34 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
 
+  const int group = num_q_heads / num_kv_heads;
+  // cascade: prefix key chunks, all non-empty (they divide the key tiles evenly)
+  int chunks = 0;
+  if (prefix_len > 0) {
+    const int nkt = (prefix_len + 127) / 128;
+    const int c = prefix_chunks(num_tokens, num_kv_heads, group, nkt);
+    const int per = (nkt + c - 1) / c;
+    chunks = (nkt + per - 1) / per;
+  }
+  float* const prefix_partials =
+      prefix_len > 0 ? reinterpret_cast<float*>(ws + lay.total) : nullptr;
+
   PlanParams pp;
   pp.qsl = query_start_loc;
   pp.seq_lens = seq_lens;
+  pp.block_tables = block_tables;
+  pp.prefix_blocks = prefix_len / kBlockSize;
   pp.num_reqs = num_reqs;
   pp.num_tokens = num_tokens;
   pp.num_kv_heads = num_kv_heads;
   pp.max_blocks_per_req = max_blocks_per_req;
   pp.max_query_len = max_query_len;
   pp.max_seq_len = max_seq_len;
-  pp.group = num_q_heads / num_kv_heads;
-  pp.use_prefill = max_query_len >= kPrefillMinQlen ? 1 : 0;
-  pp.num_workers = decode_workers(head_dim, pp.group, d->num_sms);
+  pp.group = group;
+  // a cascade sends every span to the split-KV path
+  pp.use_prefill = (prefix_len == 0 && max_query_len >= kPrefillMinQlen) ? 1 : 0;
+  const int occ_cap = prefix_len > 0 ? PA_DEC_OCC_CAP_CASCADE : PA_DEC_OCC_CAP;
+  pp.num_workers = decode_workers(head_dim, pp.group, d->num_sms, occ_cap);
   if (pp.num_workers <= 0) return PA_ERR_CUDA;
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
   pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
@@ -203,8 +240,12 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
 
-  if (pp.use_prefill) {
+  if (pp.use_prefill || prefix_len > 0) {
     PrefillLaunch pl;
+    pl.prefix_len = prefix_len;
+    pl.prefix_chunks = chunks;
+    pl.slot_floats = lay.slot_floats;
+    pl.prefix_partials = prefix_partials;
     pl.q = q;
     pl.k_cache = k_cache;
     pl.v_cache = v_cache;
@@ -222,7 +263,7 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
     pl.bt_stride = max_blocks_per_req;
     pl.scale_log2 = scale * 1.4426950408889634f;
     pl.err = d->err;
-    TimerScope timer(3, s);
+    TimerScope timer(prefix_len > 0 ? 4 : 3, s);
     const cudaError_t e = launch_prefill(pl, d->num_sms, s);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
@@ -245,15 +286,51 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
   dp.counters = pp.counters;
   dp.partials = reinterpret_cast<float*>(ws + lay.partials_off);
   dp.slot_floats = lay.slot_floats;
+  dp.key_start_blocks = prefix_len / kBlockSize;
+  dp.prefix_partials = prefix_partials;
+  dp.prefix_chunks = chunks;
+  dp.num_tokens = num_tokens;
   dp.err = d->err;
   {
     TimerScope timer(2, s);
     const cudaError_t e =
-        launch_decode(dp, head_dim, num_q_heads / num_kv_heads, d->num_sms, s);
+        launch_decode(dp, head_dim, num_q_heads / num_kv_heads, d->num_sms, occ_cap, s);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens,
+                       const int32_t* query_start_loc, float scale, void* out, int num_reqs,
+                       int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, int max_blocks_per_req,
+                       int max_query_len, int max_seq_len, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return attention_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out,
+                        num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, max_blocks_per_req, max_query_len, max_seq_len, 0, workspace,
+                        workspace_bytes, stream);
+}
+
+pa_status pa_attention_cascade(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, float scale, void* out,
+                               int num_reqs, int num_tokens, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_req, int max_query_len, int max_seq_len,
+                               int common_prefix_len, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (common_prefix_len <= 0 || common_prefix_len % kBlockSize != 0) return PA_ERR_INVALID_ARG;
+  return attention_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out,
+                        num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, max_blocks_per_req, max_query_len, max_seq_len,
+                        common_prefix_len, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_get_device_error(int* code, long long* detail, int clear) {
@@ -271,7 +348,7 @@ pa_status pa_get_device_error(int* code, long long* detail, int clear) {
 }
 
 pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event) {
-  if (kernel_id < 0 || kernel_id >= 4) return PA_ERR_INVALID_ARG;
+  if (kernel_id < 0 || kernel_id >= kNumTimers) return PA_ERR_INVALID_ARG;
   if ((start_event == nullptr) != (stop_event == nullptr)) return PA_ERR_INVALID_ARG;
   g_timer_start[kernel_id] = static_cast<cudaEvent_t>(start_event);
   g_timer_stop[kernel_id] = static_cast<cudaEvent_t>(stop_event);

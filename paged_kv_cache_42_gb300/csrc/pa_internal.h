@@ -18,9 +18,13 @@ constexpr int kMaxDecodeWorkers = 4096;
 constexpr int kPlanSmemTokens = 4096;
 
 // Split-KV workers used for W flattened positions when `all` are launched:
-// at least 8 positions each (the planner and the split-KV kernel must agree).
+// at least PA_DEC_MIN_POS positions each (the planner and the split-KV kernel
+// must agree).
+#ifndef PA_DEC_MIN_POS
+#define PA_DEC_MIN_POS 8
+#endif
 __host__ __device__ inline int plan_workers(int W, int all) {
-  int n = W / 8;
+  int n = W / PA_DEC_MIN_POS;
   return n < 1 ? 1 : (n > all ? all : n);
 }
 
@@ -86,9 +90,47 @@ __host__ __device__ inline WsLayout ws_layout(int num_reqs, int num_tokens, int 
   return l;
 }
 
+// Cascade prefix pass: work items are (pair of 128-row tiles, kv head, key
+// chunk); the prefix keys are split into as many chunks as bring the item
+// count to about this many, at most kMaxPrefixChunks. More chunks shorten the
+// prefix pass but give the split-KV kernel more partials to fold per token
+// (measured best near 40 items on the 128-token prefix-sharing batch).
+#ifndef PA_PREFIX_TARGET_ITEMS
+#define PA_PREFIX_TARGET_ITEMS 40
+#endif
+constexpr int kPrefixTargetItems = PA_PREFIX_TARGET_ITEMS;
+constexpr int kMaxPrefixChunks = 16;
+
+__host__ __device__ inline int prefix_pairs(int num_tokens, int group) {
+  const int tok_per_pair = 2 * (128 / group);
+  return (num_tokens + tok_per_pair - 1) / tok_per_pair;
+}
+// Key chunks for a prefix of `key_tiles` 128-key tiles (0: the bound used to
+// size the workspace, before the prefix length is known).
+__host__ __device__ inline int prefix_chunks(int num_tokens, int num_kv_heads, int group,
+                                             int key_tiles) {
+  const int per_chunk = prefix_pairs(num_tokens, group) * num_kv_heads;
+  int c = (kPrefixTargetItems + per_chunk - 1) / per_chunk;
+  if (c > kMaxPrefixChunks) c = kMaxPrefixChunks;
+  if (key_tiles > 0 && c > key_tiles) c = key_tiles;
+  return c < 1 ? 1 : c;
+}
+
+// Bytes of prefix partials a cascade call needs beyond the ws_layout total:
+// one partial slot per (chunk, token, kv head).
+__host__ __device__ inline size_t prefix_partials_bytes(int num_tokens, int num_q_heads,
+                                                        int num_kv_heads, int head_dim) {
+  const int G = num_q_heads / num_kv_heads;
+  const size_t slot = sizeof(float) * (size_t)(16 + G * head_dim);
+  return pa_align256(slot * (size_t)prefix_chunks(num_tokens, num_kv_heads, G, 0) *
+                     (size_t)num_tokens * (size_t)num_kv_heads);
+}
+
 struct PlanParams {
   const int32_t* qsl;
   const int32_t* seq_lens;
+  const int32_t* block_tables;  // read only for the cascade prefix check
+  int prefix_blocks;            // cascade: blocks of the common prefix; 0 otherwise
   int num_reqs, num_tokens, num_kv_heads, max_blocks_per_req, max_query_len, max_seq_len;
   int group;        // G = Hq / Hkv
   int use_prefill;  // route requests with qlen >= kPrefillMinQlen to the tensor-core kernel
@@ -103,6 +145,11 @@ struct PlanParams {
 };
 
 struct PrefillLaunch {
+  // cascade prefix pass (prefix_len > 0): no planner tiles; items are
+  // (pair, kv head, key chunk) over request 0's first prefix_len keys and the
+  // output is fp32 partials, one slot per (chunk, token, kv head)
+  int prefix_len, prefix_chunks, slot_floats;
+  float* prefix_partials;
   const void* q;
   const void* k_cache;
   const void* v_cache;
@@ -131,6 +178,10 @@ struct DecodeParams {
   int* counters;
   float* partials;
   int slot_floats;
+  // cascade: keys start after the common prefix, whose partials are merged in
+  int key_start_blocks;          // 0 without a cascade
+  const float* prefix_partials;  // null without a cascade
+  int prefix_chunks, num_tokens;
   unsigned long long* err;
 };
 
@@ -154,12 +205,23 @@ __device__ inline void report_error(unsigned long long* err, int code, long long
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
-// grid_ctas is filled with the grid actually used. head_dim / G select the
-// instantiation; unsupported combinations return cudaErrorInvalidValue.
+// head_dim / G select the instantiation; unsupported combinations return
+// cudaErrorInvalidValue. occ_cap bounds the resident CTAs per SM (the grid is
+// SMs x min(occupancy, occ_cap)).
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
-                          cudaStream_t s);
+                          int occ_cap, cudaStream_t s);
 // Split-KV workers launch_decode will use on this device (0 on error).
-int decode_workers(int head_dim, int group, int num_sms);
+int decode_workers(int head_dim, int group, int num_sms, int occ_cap);
+
+// Resident split-KV CTAs per SM: two suit long per-token key ranges (each
+// worker's slice stays long); the short suffixes of a cascade call run better
+// with a third, which hides more latency.
+#ifndef PA_DEC_OCC_CAP
+#define PA_DEC_OCC_CAP 2
+#endif
+#ifndef PA_DEC_OCC_CAP_CASCADE
+#define PA_DEC_OCC_CAP_CASCADE 3
+#endif
 cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s);
 
 }  // namespace pa

@@ -9,6 +9,10 @@
 //    prefix sum of Hkv * ceil(keys / 16) positions, which the split-KV
 //    kernel's workers slice into equal parts.
 //  - The merge counters of every (unit, kv head) are zeroed.
+//  - Cascade calls (common prefix of prefix_blocks blocks): every span goes
+//    to the split-KV path with the prefix blocks left out of its positions;
+//    requests must see the whole prefix and start with request 0's prefix
+//    blocks, which is checked here.
 // Invalid spans or lengths are skipped and reported on the device error word.
 #include "pa_internal.h"
 #include "ptx.cuh"
@@ -80,7 +84,8 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     qlen = q1 - q0;
     L = p.seq_lens[r];
     if (L < qlen || (L + kBlockSize - 1) / kBlockSize > p.max_blocks_per_req ||
-        qlen > p.max_query_len || L > p.max_seq_len) {
+        qlen > p.max_query_len || L > p.max_seq_len ||
+        L - qlen < p.prefix_blocks * kBlockSize) {
       if (report) report_error(p.err, PA_DEVERR_LENGTHS, r);
       return false;
     }
@@ -91,6 +96,14 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     return last / 128 + 1;
   };
 
+  if (p.prefix_blocks > 0) {  // every table starts with request 0's prefix blocks
+    const long long n = (long long)(p.num_reqs - 1) * p.prefix_blocks;
+    for (long long i = threadIdx.x; i < n; i += blockDim.x) {
+      const int r = 1 + (int)(i / p.prefix_blocks), b = (int)(i % p.prefix_blocks);
+      if (p.block_tables[(size_t)r * p.max_blocks_per_req + b] != p.block_tables[b])
+        report_error(p.err, PA_DEVERR_PREFIX, r);
+    }
+  }
   for (int r = threadIdx.x; r < p.num_reqs; r += blockDim.x) {
     int q0, qlen, L;
     if (!check(r, q0, qlen, L, true)) continue;
@@ -130,7 +143,8 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   for (int c0 = 0; c0 < T; c0 += blockDim.x) {
     const int t = c0 + threadIdx.x;
     const int2 u = t < T ? raw[t] : make_int2(-1, 0);
-    const int nb = (u.y + kBlockSize - 1) / kBlockSize;
+    // blocks on the split-KV path: all the token sees, less a cascade prefix
+    const int nb = max(0, (u.y + kBlockSize - 1) / kBlockSize - p.prefix_blocks);
     const long long packed = ((long long)(nb > 0) << 40) | ((long long)nb * p.num_kv_heads);
     long long total;
     const long long ex = block_exclusive_scan(packed, &total, scan_sm);  // syncs: raw reads done

@@ -29,6 +29,15 @@
 // by more than 2^8; otherwise P is formed against the stale max, which keeps
 // every P <= 256 and the result exact up to rounding.
 //
+// Cascade prefix pass (the PREFIX instantiation; "vLLM: An Exhaustive
+// Technical Study for Kernel Engineers", 2.3, cascade attention): the same
+// pipeline over the common prefix shared by every request of the batch. A
+// work item is (pair of row tiles of consecutive batch tokens, kv head, chunk
+// of prefix key tiles); every row sees every prefix key (the prefix lies in
+// each request's context), and the epilogue writes an fp32 partial (running
+// max, sum, unnormalised output) per (chunk, token, kv head) for the split-KV
+// kernel to merge, instead of bf16 rows.
+//
 // Warp roles (320 threads): warp 0 issues TMA loads (both Q tiles per work
 // item, K into a 3-stage ring released right after both S MMAs of a key tile,
 // V into a 2-stage ring released after both P*V), warp 1 allocates TMEM and
@@ -96,10 +105,54 @@ struct PrefillParams {
   const PrefillTile* tiles;
   int bt_stride, num_q_heads, num_kv_heads, num_blocks;
   float scale_log2;
+  // cascade prefix pass
+  int num_tokens, prefix_len, prefix_chunks, prefix_pairs, slot_floats;
+  float* prefix_partials;
   unsigned long long* err;
 };
 
-template <int D, int G>
+// One work item as every role sees it.
+struct Item {
+  int req;    // block-table row (request 0 for the prefix pass)
+  int kv;     // kv head
+  int j0;     // first chunk token of the pair (prefill)
+  int i0, n;  // key tiles i0 .. i0 + n - 1
+  int L;      // keys that exist (sequence length; prefix length)
+  int tok0;   // batch token of the pair's first row
+  int chunk;  // key chunk (prefix pass)
+};
+
+template <int D, int G, bool PREFIX>
+__device__ __forceinline__ Item get_item(const PrefillParams& p, int t) {
+  using C = PCfg<D, G>;
+  Item it;
+  if constexpr (PREFIX) {
+    const int nkt = (p.prefix_len + 127) / 128;
+    const int per = (nkt + p.prefix_chunks - 1) / p.prefix_chunks;
+    it.kv = t % p.num_kv_heads;
+    const int rest = t / p.num_kv_heads;
+    it.chunk = rest % p.prefix_chunks;
+    it.req = 0;
+    it.j0 = 0;
+    it.i0 = it.chunk * per;
+    it.n = min(per, nkt - it.i0);  // >= 1: the host picks chunks that are all non-empty
+    it.L = p.prefix_len;
+    it.tok0 = (rest / p.prefix_chunks) * 2 * C::TOK;
+  } else {
+    const PrefillTile tl = p.tiles[t];
+    it.req = tl.req;
+    it.kv = tl.kv;
+    it.j0 = tl.j0;
+    it.i0 = 0;
+    it.n = tl.nkv;
+    it.L = __ldg(p.seq_lens + tl.req);
+    it.tok0 = __ldg(p.qsl + tl.req) + tl.j0;
+    it.chunk = 0;
+  }
+  return it;
+}
+
+template <int D, int G, bool PREFIX>
 __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PCfg<D, G>;
   extern __shared__ unsigned char smem_raw[];
@@ -129,8 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  griddep_wait();  // the work list comes from the preceding (planner) grid
-  const int ntiles = p.header->num_tiles;
+  // The work list comes from the preceding (planner) grid. The prefix pass
+  // needs none of it and waits only before it completes (see the end).
+  if constexpr (!PREFIX) griddep_wait();
+  const int ntiles =
+      PREFIX ? p.prefix_pairs * p.num_kv_heads * p.prefix_chunks : p.header->num_tiles;
 
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8 * i; };
   auto wait = [&](int i, uint32_t parity) -> bool {
@@ -146,13 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
     int g = 0, it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
-      const PrefillTile tl = p.tiles[t];
-      const int q0 = __ldg(p.qsl + tl.req);
-      const int L = __ldg(p.seq_lens + tl.req);
-      const int nb = (L + kBlockSize - 1) / kBlockSize;
+      const Item tl = get_item<D, G, PREFIX>(p, t);
+      const int nb = (tl.L + kBlockSize - 1) / kBlockSize;
       const int32_t* const bt_row = p.block_tables + (size_t)tl.req * p.bt_stride;
-      auto load_group = [&](int grp) -> int {
-        const int b = grp * 32 + lane;
+      auto load_group = [&](int grp) -> int {  // blocks of key tiles i0 + 4 grp .. + 3
+        const int b = tl.i0 * 8 + grp * 32 + lane;
         if (b >= nb) return -1;
         const int pid = __ldg(bt_row + b);
         if (pid < 0 || pid >= p.num_blocks) {
@@ -162,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         return pid;
       };
       int pid_cur = load_group(0);
-      int pid_nxt = tl.nkv > 4 ? load_group(1) : -1;
+      int pid_nxt = tl.n > 4 ? load_group(1) : -1;
       if (it > 0 && !wait(B_Q_EMPTY, (it - 1) & 1)) { ok = false; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(BAR(B_Q_FULL), 2 * C::Q_BYTES);
@@ -171,12 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(base + C::OFF_Q + rt * C::Q_BYTES + c * C::CHUNK, &p.tm_q, c * 64,
-                        tl.kv * G, q0 + tl.j0 + rt * C::TOK, BAR(B_Q_FULL));
+                        tl.kv * G, tl.tok0 + rt * C::TOK, BAR(B_Q_FULL));
       }
-      for (int i = 0; i < tl.nkv; ++i, ++g) {
+      for (int i = 0; i < tl.n; ++i, ++g) {
         if (i > 0 && (i & 3) == 0) {
           pid_cur = pid_nxt;
-          pid_nxt = (i + 4 < tl.nkv) ? load_group((i >> 2) + 1) : -1;
+          pid_nxt = (i + 4 < tl.n) ? load_group((i >> 2) + 1) : -1;
         }
         const int ks = g % C::KSTAGES, vs = g % C::VSTAGES;
         const int pid = __shfl_sync(kAll, pid_cur, ((i & 3) << 3) + (lane & 7));
@@ -217,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
     int it = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
-      const PrefillTile tl = p.tiles[t];
-      const int L = __ldg(p.seq_lens + tl.req);
+      const Item tl = get_item<D, G, PREFIX>(p, t);
+      const int L = tl.L;
       if (!wait(B_Q_FULL, it & 1)) { ok = false; break; }
 
       // S_rt(key tile of counter gk) for row tile rt
@@ -252,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         ++np[rt];
         if (rt == 0) {
           if (!wait(B_V_FULL + vst, (gv / C::VSTAGES) & 1)) return false;
-          const int kv0 = i * 128;
+          const int kv0 = (tl.i0 + i) * 128;
           if (kv0 + 128 > L) {
             // Rows of keys past the sequence end may hold anything (NaN too);
             // their P is 0, but 0 * NaN would poison O, so clear them.
@@ -286,10 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         return true;
       };
 
-      ok = issue_s(0, tl.nkv == 1) && issue_s(1, tl.nkv == 1);
-      for (int i = 0; ok && i < tl.nkv; ++i) {
-        const bool more = i + 1 < tl.nkv;
-        const bool last_next = i + 2 == tl.nkv;
+      ok = issue_s(0, tl.n == 1) && issue_s(1, tl.n == 1);
+      for (int i = 0; ok && i < tl.n; ++i) {
+        const bool more = i + 1 < tl.n;
+        const bool last_next = i + 2 == tl.n;
         ok = issue_pv(0, i);
         if (ok && more) ok = issue_s(0, last_next);
         if (ok) ok = issue_pv(1, i);
@@ -311,21 +365,25 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
     int ns = 0, it = 0;  // S_rt events consumed; work items done
     bool ok = true;
     for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
-      const PrefillTile tl = p.tiles[t];
-      const int q0 = __ldg(p.qsl + tl.req);
-      const int qlen = __ldg(p.qsl + tl.req + 1) - q0;
-      const int L = __ldg(p.seq_lens + tl.req);
-      const int ctx = L - qlen;
-      const int j = tl.j0 + rt * C::TOK + m / G;  // chunk token of this row
-      const int lim = min(ctx + j, L - 1);         // last key this row may see
+      const Item tl = get_item<D, G, PREFIX>(p, t);
+      const int L = tl.L;
+      int qlen = 0, j = 0, lim;
+      if constexpr (PREFIX) {
+        lim = L - 1;  // the whole prefix, for every row
+      } else {
+        qlen = __ldg(p.qsl + tl.req + 1) - __ldg(p.qsl + tl.req);
+        const int ctx = L - qlen;
+        j = tl.j0 + rt * C::TOK + m / G;  // chunk token of this row
+        lim = min(ctx + j, L - 1);        // last key this row may see
+      }
       float m_used = -INFINITY, l = 0.f;
-      for (int i = 0; i < tl.nkv; ++i) {
+      for (int i = 0; i < tl.n; ++i) {
         // S_rt(i) complete implies every earlier MMA is too: O_rt is stable
         // and P_rt(i-1) has been consumed.
         if (!wait(B_S_FULL + rt, ns & 1)) { ok = false; break; }
         ++ns;
         tc_fence_after();
-        const int kv0 = i * 128;
+        const int kv0 = (tl.i0 + i) * 128;
         const bool unmasked = __all_sync(kAll, kv0 + 127 <= lim);
         // pass 1: row max of the raw scores over visible keys
         float mx = -INFINITY;
@@ -347,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         float alpha = 1.f;
         bool resc = false;
         if (i == 0) {
-          m_used = mt;  // key 0 is always visible: finite
+          m_used = mt;  // the item's first key is always visible: finite
         } else if (mt > m_used + 8.f) {
           alpha = exp2f(m_used - mt);
           m_used = mt;
@@ -408,10 +466,40 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
       // ---- epilogue: O / l -> bf16 rows of out ----
       if (!wait(B_PV_DONE + rt, (ns - 1) & 1)) { ok = false; break; }
       tc_fence_after();
+      if constexpr (PREFIX) {
+        // fp32 partial of (chunk, token, kv head), head m % G of the slot
+        const int tok = tl.tok0 + rt * C::TOK + m / G;
+        const int h = m % G;
+        const bool store = tok < p.num_tokens;
+        float* const slot = p.prefix_partials +
+                            (((size_t)tl.chunk * p.num_tokens + (store ? tok : 0)) *
+                                 p.num_kv_heads + tl.kv) * p.slot_floats;
+        if (store) {
+          __stcg(slot + h, m_used);
+          __stcg(slot + G + h, l);
+        }
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_addr + c * 32, o);
+          tmem_wait_ld();
+          if (store) {
+            float* const dst = slot + 16 + h * D + c * 32;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              __stcg(reinterpret_cast<float4*>(dst + 4 * v),
+                     make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                 __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(B_O_EMPTY + rt));
+        continue;
+      }
       const float inv = 1.f / l;
       const bool store = j < qlen;
       uint16_t* const orow =
-          p.out + ((size_t)(q0 + j) * p.num_q_heads + (size_t)tl.kv * G + (m % G)) * D;
+          p.out + ((size_t)(tl.tok0 - tl.j0 + j) * p.num_q_heads + (size_t)tl.kv * G + (m % G)) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -434,6 +522,13 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
     }
   }
 
+  if constexpr (PREFIX) {
+    // The split-KV grid launched after this one may start; this grid does not
+    // complete before the planner (and the KV write before it) has, so a
+    // dependent that waits for this grid sees the plan too.
+    griddep_launch_dependents();
+    griddep_wait();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -472,7 +567,7 @@ bool encode_bf16(CUtensorMap* m, int rank, const void* ptr, const cuuint64_t* di
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int G>
+template <int D, int G, bool PREFIX>
 cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
   using C = PCfg<D, G>;
   PrefillParams p;
@@ -502,8 +597,19 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
   p.num_blocks = a.num_blocks;
   p.scale_log2 = a.scale_log2;
   p.err = a.err;
+  p.num_tokens = a.num_tokens;
+  p.prefix_len = a.prefix_len;
+  p.prefix_chunks = a.prefix_chunks;
+  p.prefix_pairs = prefix_pairs(a.num_tokens, G);
+  p.slot_floats = a.slot_floats;
+  p.prefix_partials = a.prefix_partials;
+  int grid = num_sms;
+  if (PREFIX) {
+    const int items = p.prefix_pairs * a.num_kv_heads * a.prefix_chunks;
+    grid = items < num_sms ? items : num_sms;
+  }
 
-  auto kern = pa_prefill_kernel<D, G>;
+  auto kern = pa_prefill_kernel<D, G, PREFIX>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -514,7 +620,7 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(num_sms);
+  cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
@@ -528,25 +634,31 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
-  if (!get_encoder()) return cudaErrorNotSupported;
+template <bool PREFIX>
+cudaError_t launch_prefill_mode(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
   const int G = a.num_q_heads / a.num_kv_heads;
   if (a.head_dim == 128) {
     switch (G) {
-      case 1: return launch_prefill_t<128, 1>(a, num_sms, s);
-      case 2: return launch_prefill_t<128, 2>(a, num_sms, s);
-      case 4: return launch_prefill_t<128, 4>(a, num_sms, s);
-      case 8: return launch_prefill_t<128, 8>(a, num_sms, s);
+      case 1: return launch_prefill_t<128, 1, PREFIX>(a, num_sms, s);
+      case 2: return launch_prefill_t<128, 2, PREFIX>(a, num_sms, s);
+      case 4: return launch_prefill_t<128, 4, PREFIX>(a, num_sms, s);
+      case 8: return launch_prefill_t<128, 8, PREFIX>(a, num_sms, s);
     }
   } else if (a.head_dim == 64) {
     switch (G) {
-      case 1: return launch_prefill_t<64, 1>(a, num_sms, s);
-      case 2: return launch_prefill_t<64, 2>(a, num_sms, s);
-      case 4: return launch_prefill_t<64, 4>(a, num_sms, s);
-      case 8: return launch_prefill_t<64, 8>(a, num_sms, s);
+      case 1: return launch_prefill_t<64, 1, PREFIX>(a, num_sms, s);
+      case 2: return launch_prefill_t<64, 2, PREFIX>(a, num_sms, s);
+      case 4: return launch_prefill_t<64, 4, PREFIX>(a, num_sms, s);
+      case 8: return launch_prefill_t<64, 8, PREFIX>(a, num_sms, s);
     }
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
+  if (!get_encoder()) return cudaErrorNotSupported;
+  return a.prefix_len > 0 ? launch_prefill_mode<true>(a, num_sms, s)
+                          : launch_prefill_mode<false>(a, num_sms, s);
 }
 
 }  // namespace pa
