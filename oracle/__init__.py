@@ -41,6 +41,18 @@ def load(mutant: int = 0, out_dir: str | None = None) -> ctypes.CDLL:
                                          i, i, i, i, i, i, p, i, i]
         lib.oracle_attention.restype = i
         lib.oracle_mutant_id.restype = i
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_quantize.argtypes = [p, ctypes.c_float, p, ctypes.c_int64]
+        lib.oracle_e4m3_quantize.restype = None
+        lib.oracle_write_kv_fp8.argtypes = [p, p, p, p, p, ctypes.c_float, ctypes.c_float,
+                                            i, i, i, i, i]
+        lib.oracle_write_kv_fp8.restype = i
+        lib.oracle_attention_fp8.argtypes = [p, p, p, ctypes.c_double, ctypes.c_double, p, i, p,
+                                             p, ctypes.c_double, p, i, i, i, i, i, i, p, i, i]
+        lib.oracle_attention_fp8.restype = i
         _LIBS[key] = lib
     return _LIBS[key]
 
@@ -96,6 +108,73 @@ def attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scal
                               hq, hkv, d, bs, nb,
                               None if rl is None else _ptr(rl),
                               0 if rl is None else int(rl.shape[0]), int(threads))
+    if st:
+        raise OracleError(_ERRORS.get(st, str(st)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+# ---------------------------------------------------------------------------
+def e4m3_value(code: int, *, lib=None) -> float:
+    """Value of one E4M3 code (OCP 8-bit format, max 448, no infinities)."""
+    return float((lib or load()).oracle_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_encode(y: float, *, lib=None) -> int:
+    """Nearest E4M3 code to the binary32 value y (ties to even, saturating)."""
+    return int((lib or load()).oracle_e4m3_encode(float(y)))
+
+
+def e4m3_quantize(x_bits, scale: float, *, lib=None) -> np.ndarray:
+    """E4M3 codes of bf16 values x / scale (quotient in binary32)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib.oracle_e4m3_quantize(_ptr(x), float(scale), _ptr(out), int(x.size))
+    return out
+
+
+def write_kv_fp8(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: float, *,
+                 lib=None) -> None:
+    """Quantising scatter into uint8 E4M3 caches [num_blocks, Hkv, bs, D], in place."""
+    lib = lib or load()
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    nb, hkv, bs, d = k_cache.shape
+    st = lib.oracle_write_kv_fp8(_ptr(k), _ptr(v), _ptr(sm), _ptr(k_cache), _ptr(v_cache),
+                                 float(k_scale), float(v_scale), int(sm.shape[0]), hkv, d, bs, nb)
+    if st:
+        raise OracleError(_ERRORS.get(st, str(st)))
+
+
+def attention_fp8(q, k_cache, v_cache, k_scale: float, v_scale: float, block_tables, seq_lens,
+                  query_start_loc, scale, *, reqs=None, threads: int | None = None, out=None,
+                  lib=None) -> np.ndarray:
+    """Attention over E4M3 caches (keys code * k_scale, values code * v_scale),
+    in float64; otherwise as :func:`attention`."""
+    lib = lib or load()
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8
+    T, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    assert d == d2
+    if out is None:
+        out = np.full((T, hq, d), np.nan, dtype=np.float64)
+    rl = None
+    if reqs is not None:
+        rl = np.ascontiguousarray(np.asarray(reqs, dtype=np.int32))
+    threads = threads or os.cpu_count() or 1
+    st = lib.oracle_attention_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), float(k_scale),
+                                  float(v_scale), _ptr(bt), int(bt.shape[1]), _ptr(sl), _ptr(qsl),
+                                  float(scale), _ptr(out), int(sl.shape[0]), hq, hkv, d, bs, nb,
+                                  None if rl is None else _ptr(rl),
+                                  0 if rl is None else int(rl.shape[0]), int(threads))
     if st:
         raise OracleError(_ERRORS.get(st, str(st)))
     return out

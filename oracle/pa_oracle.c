@@ -32,6 +32,17 @@
  *     w_p = exp(s_p - m); o = sum_p w_p v_p / sum_p w_p.
  *     Everything is evaluated in double precision in sequence order.
  *
+ *  3. FP8 KV cache ("vLLM: An Exhaustive Technical Study for Kernel Engineers",
+ *     2.8, the KV-cache quantization paragraph: --kv-cache-dtype fp8 means
+ *     E4M3 with an fp32 per-tensor scale, k_scale for K and v_scale for V).
+ *     Writing stores code = E4M3(x / scale), the quotient taken in binary32
+ *     (as the GPU takes it) and rounded to the nearest E4M3 value, ties to
+ *     even, magnitudes beyond the largest finite value saturating to it.
+ *     Reading uses value(code) * scale. E4M3 here is the OCP 8-bit format
+ *     the GPU implements: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits,
+ *     no infinities, S.1111.111 the only NaN pattern, largest finite 448.
+ *     Attention over an FP8 cache is item 2 on the dequantised values.
+ *
  * bf16 values are passed as their raw 16-bit patterns; the widening to double
  * is exact (a bf16 is the top half of an IEEE binary32).
  *
@@ -68,6 +79,56 @@ static double widen_bf16(uint16_t bits) {
   return (double)f;
 }
 
+/* ---- E4M3 ---------------------------------------------------------------- */
+
+/* Value of an E4M3 code: (-1)^s * 2^(e-7) * (1 + m/8) for e > 0, and
+ * (-1)^s * 2^-6 * (m/8) for e == 0 (subnormals); S.1111.111 is NaN. */
+double oracle_e4m3_value(uint8_t c) {
+  const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+#if ORACLE_MUTANT == 9
+  const double mag = e == 0 ? ldexp((double)m, -10) : ldexp((double)(8 + m), e - 11); /* bias 8 */
+#else
+  const double mag = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+#endif
+  return sgn ? -mag : mag;
+}
+
+/* Nearest E4M3 code to y (ties to even), saturating at +-448; NaN to NaN. */
+uint8_t oracle_e4m3_encode(float y) {
+  if (isnan(y)) return signbit(y) ? 0xFF : 0x7F;
+  const uint8_t sgn = signbit(y) ? 0x80 : 0x00;
+  const double a = fabs((double)y);
+  if (a >= 448.0) return sgn | 0x7E;
+  /* the spacing of E4M3 values around a: 2^-9 below 2^-6 (subnormals),
+   * else 2^(E-3) in the binade [2^E, 2^(E+1)) */
+  int e2;
+  frexp(a, &e2);
+  const int E = e2 - 1;
+  const double quantum = E < -6 ? ldexp(1.0, -9) : ldexp(1.0, E - 3);
+#if ORACLE_MUTANT == 8
+  const double n = floor(a / quantum); /* rounding toward zero */
+#else
+  const double n = nearbyint(a / quantum); /* round half to even (default mode) */
+#endif
+  const double q = n * quantum;            /* the chosen E4M3 magnitude */
+  if (q == 0.0) return sgn;
+  if (q < ldexp(1.0, -6)) return (uint8_t)(sgn | (uint8_t)n); /* subnormal: m = n */
+  frexp(q, &e2);
+  const int Eq = e2 - 1;
+  const int m = (int)(q / ldexp(1.0, Eq - 3)) - 8;
+  return (uint8_t)(sgn | (uint8_t)((Eq + 7) << 3) | (uint8_t)m);
+}
+
+/* Quantise n bf16 values with one scale: code = E4M3(binary32(x / scale)). */
+void oracle_e4m3_quantize(const uint16_t* x, float scale, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    const float xf = (float)widen_bf16(x[i]);
+    const float y = xf / scale; /* binary32 division, as on the GPU */
+    out[i] = oracle_e4m3_encode(y);
+  }
+}
+
 int oracle_write_kv(const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
                     uint16_t* k_cache, uint16_t* v_cache, int num_tokens, int num_kv_heads,
                     int head_dim, int block_size, int num_blocks) {
@@ -95,10 +156,37 @@ int oracle_write_kv(const uint16_t* k, const uint16_t* v, const int64_t* slot_ma
   return OR_OK;
 }
 
+/* KV write into E4M3 caches [num_blocks][num_kv_heads][block_size][head_dim]. */
+int oracle_write_kv_fp8(const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
+                        uint8_t* k_cache, uint8_t* v_cache, float k_scale, float v_scale,
+                        int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                        int num_blocks) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0 ||
+      !(k_scale > 0.0f) || !(v_scale > 0.0f))
+    return OR_BAD_ARG;
+  const int64_t num_slots = (int64_t)num_blocks * block_size;
+  for (int t = 0; t < num_tokens; ++t)
+    if (slot_mapping[t] >= num_slots) return OR_BAD_SLOT;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t s = slot_mapping[t];
+    if (s < 0) continue;
+    const int64_t blk = s / block_size, off = s % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * head_dim;
+      const int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim;
+      oracle_e4m3_quantize(k + src, k_scale, k_cache + dst, head_dim);
+      oracle_e4m3_quantize(v + src, v_scale, v_cache + dst, head_dim);
+    }
+  }
+  return OR_OK;
+}
+
 typedef struct {
   const uint16_t* q;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
+  const void* k_cache;  /* bf16 patterns, or E4M3 codes when kv_fp8 */
+  const void* v_cache;
+  int kv_fp8;
+  double k_scale, v_scale;
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
@@ -145,8 +233,15 @@ static int run_item(oracle_job* job, int item, double* Kr, double* Vr, double* w
     if (blk < 0 || blk >= job->num_blocks) return OR_BAD_BLOCK;
     const int64_t base = (((int64_t)blk * Hkv + kvh) * bs + off) * D;
     for (int d = 0; d < D; ++d) {
-      Kr[(int64_t)p * D + d] = widen_bf16(job->k_cache[base + d]);
-      Vr[(int64_t)p * D + d] = widen_bf16(job->v_cache[base + d]);
+      if (job->kv_fp8) {
+        Kr[(int64_t)p * D + d] =
+            oracle_e4m3_value(((const uint8_t*)job->k_cache)[base + d]) * job->k_scale;
+        Vr[(int64_t)p * D + d] =
+            oracle_e4m3_value(((const uint8_t*)job->v_cache)[base + d]) * job->v_scale;
+      } else {
+        Kr[(int64_t)p * D + d] = widen_bf16(((const uint16_t*)job->k_cache)[base + d]);
+        Vr[(int64_t)p * D + d] = widen_bf16(((const uint16_t*)job->v_cache)[base + d]);
+      }
     }
   }
 
@@ -238,11 +333,12 @@ static void* worker(void* arg) {
 
 /* out: double [num_tokens][num_q_heads][head_dim]; rows of requests not in the
  * list are left untouched. reqs == NULL evaluates every request. */
-int oracle_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                     const int32_t* block_tables, int bt_stride, const int32_t* seq_lens,
-                     const int32_t* query_start_loc, double scale, double* out, int num_reqs,
-                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                     int num_blocks, const int32_t* reqs, int n_reqs_listed, int num_threads) {
+static int attention_job(const uint16_t* q, const void* k_cache, const void* v_cache, int kv_fp8,
+                         double k_scale, double v_scale, const int32_t* block_tables,
+                         int bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                         double scale, double* out, int num_reqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         const int32_t* reqs, int n_reqs_listed, int num_threads) {
   if (num_reqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       block_size <= 0 || num_q_heads % num_kv_heads != 0)
     return OR_BAD_ARG;
@@ -260,6 +356,7 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t*
   oracle_job job;
   memset(&job, 0, sizeof job);
   job.q = q; job.k_cache = k_cache; job.v_cache = v_cache;
+  job.kv_fp8 = kv_fp8; job.k_scale = k_scale; job.v_scale = v_scale;
   job.block_tables = block_tables; job.seq_lens = seq_lens; job.qsl = query_start_loc;
   job.reqs = reqs; job.n_reqs_listed = n_reqs_listed; job.scale = scale; job.out = out;
   job.bt_stride = bt_stride; job.num_q_heads = num_q_heads; job.num_kv_heads = num_kv_heads;
@@ -282,6 +379,30 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t*
   pthread_mutex_destroy(&job.lock);
   free(all);
   return job.status;
+}
+
+int oracle_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                     const int32_t* block_tables, int bt_stride, const int32_t* seq_lens,
+                     const int32_t* query_start_loc, double scale, double* out, int num_reqs,
+                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                     int num_blocks, const int32_t* reqs, int n_reqs_listed, int num_threads) {
+  return attention_job(q, k_cache, v_cache, 0, 1.0, 1.0, block_tables, bt_stride, seq_lens,
+                       query_start_loc, scale, out, num_reqs, num_q_heads, num_kv_heads, head_dim,
+                       block_size, num_blocks, reqs, n_reqs_listed, num_threads);
+}
+
+/* Attention over E4M3 caches: keys value(code) * k_scale, values
+ * value(code) * v_scale, otherwise as oracle_attention. */
+int oracle_attention_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                         double k_scale, double v_scale, const int32_t* block_tables,
+                         int bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                         double scale, double* out, int num_reqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         const int32_t* reqs, int n_reqs_listed, int num_threads) {
+  if (!(k_scale > 0.0) || !(v_scale > 0.0)) return OR_BAD_ARG;
+  return attention_job(q, k_cache, v_cache, 1, k_scale, v_scale, block_tables, bt_stride,
+                       seq_lens, query_start_loc, scale, out, num_reqs, num_q_heads, num_kv_heads,
+                       head_dim, block_size, num_blocks, reqs, n_reqs_listed, num_threads);
 }
 
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }
