@@ -49,6 +49,7 @@ METRIC = "paged-attn decode KV GB/s (frac of HBM peak); mixed-batch tokens/s per
 HEADLINE_CONFIG = 2
 MIXED_CONFIG = 3
 PREFIX_CONFIG = 4
+FP8_SCALES = (0.0113, 0.0127)  # k_scale, v_scale of the E4M3 cache runs
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -211,11 +212,12 @@ class Resident:
     """A workload resident on the device plus the pinned host copies used by
     the end-to-end measurement."""
 
-    def __init__(self, w: wl.Workload, torch, binding, cascade_len: int = 0):
+    def __init__(self, w: wl.Workload, torch, binding, cascade_len: int = 0, fp8_scales=None):
         self.w = w
         self.torch = torch
         self.binding = binding
         self.cascade_len = cascade_len  # > 0: attention through pa_attention_cascade
+        self.fp8 = fp8_scales           # (k_scale, v_scale): an E4M3 cache
         dev = torch.device("cuda")
 
         def bf(bits):
@@ -232,6 +234,13 @@ class Resident:
         self.d = {k: v.to(dev) for k, v in self.h.items()}
         self.k_cache = bf(w.k_cache).to(dev)
         self.v_cache = bf(w.v_cache).to(dev)
+        if self.fp8:
+            # the cached context as E4M3 codes (torch's own conversion: set-up only)
+            def codes(c, scale):
+                x = (c.float() / scale).clamp(-448.0, 448.0)
+                return x.to(torch.float8_e4m3fn).view(torch.uint8)
+            self.k_cache = codes(self.k_cache, self.fp8[0])
+            self.v_cache = codes(self.v_cache, self.fp8[1])
         self.out = torch.empty_like(self.d["q"])
         self.h_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
         wsize = binding.cascade_workspace_size if cascade_len else binding.workspace_size
@@ -242,6 +251,13 @@ class Resident:
 
     def step(self):
         d, w, b = self.d, self.w, self.binding
+        if self.fp8:
+            ks, vs = self.fp8
+            b.write_kv_fp8(d["k"], d["v"], d["slot_mapping"], self.k_cache, self.v_cache, ks, vs)
+            b.attention_fp8(d["q"], self.k_cache, self.v_cache, d["block_tables"], d["seq_lens"],
+                            d["qsl"], w.scale, ks, vs, max_query_len=w.max_query_len,
+                            max_seq_len=w.max_seq_len, out=self.out, workspace=self.ws)
+            return
         b.write_kv(d["k"], d["v"], d["slot_mapping"], self.k_cache, self.v_cache)
         if self.cascade_len:
             b.attention_cascade(d["q"], self.k_cache, self.v_cache, d["block_tables"],
@@ -343,6 +359,32 @@ def prefix_share_timing(args, flush, torch, binding, dist, rank, world) -> dict:
     return out
 
 
+def fp8_timing(args, flush, torch, binding, dist, rank, world, peaks) -> dict:
+    """The headline decode batch with an E4M3 KV cache (per-tensor scales)."""
+    w = wl.make_config(HEADLINE_CONFIG, seed=42 + HEADLINE_CONFIG + 1000 * rank)
+    sb = step_bytes(w)
+    kv8 = sb["kv"] // 2
+    attn8 = sb["attention"] - sb["kv"] + kv8
+    steps = max(50, args.steps // 10)
+    res = Resident(w, torch, binding, fp8_scales=FP8_SCALES)
+    t = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
+    code, detail = binding.get_device_error(clear=True)
+    if code:
+        raise RuntimeError(f"device error {code} at {detail}")
+    ms = max_over_ranks(t["ms_per_step"], dist)
+    dec = max_over_ranks(t["decode_ms"], dist)
+    del res
+    torch.cuda.empty_cache()
+    achieved = attn8 / (dec * 1e-3) / 1e9
+    return {"workload": f"{wl.CONFIG_NAMES[HEADLINE_CONFIG]} with an E4M3 KV cache "
+                        "(k_scale 0.0113, v_scale 0.0127)",
+            "steps": steps, "ms_per_step": round(ms, 5), "decode_kernel_ms": round(dec, 5),
+            "kv_bytes": kv8, "algorithmic_bytes_per_launch": attn8,
+            "achieved_gbs": round(achieved, 1), "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "peak_source": peaks["source"],
+            "requests_per_s": round(world * w.num_reqs / (ms * 1e-3), 1)}
+
+
 def run_ours(args, rank, world, local, dist):
     import torch
 
@@ -371,7 +413,8 @@ def run_ours(args, rank, world, local, dist):
                                 else []):
         w = wl.make_config(idx, seed=42 + idx + 1000 * rank)
         casc = w.shared_prefix_blocks * 16 if (args.cascade and idx == args.config) else 0
-        res = Resident(w, torch, binding, cascade_len=casc)
+        f8 = FP8_SCALES if (args.fp8 and idx == args.config) else None
+        res = Resident(w, torch, binding, cascade_len=casc, fp8_scales=f8)
         sb = step_bytes(w)
         steps = args.steps if idx == args.config else max(50, args.steps // 10)
         t = time_steps(res, steps, args.warmup, flush, torch, binding, dist,
@@ -450,6 +493,8 @@ def run_ours(args, rank, world, local, dist):
             "kv_bytes": m["sb"]["kv"], "prefill_causal_flops": prefill_flops(mw)}
     if not args.quick and args.config != PREFIX_CONFIG:
         line["prefix_share"] = prefix_share_timing(args, flush, torch, binding, dist, rank, world)
+    if not args.quick:
+        line["kv_fp8"] = fp8_timing(args, flush, torch, binding, dist, rank, world, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0 and not args.quick:
@@ -582,6 +627,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=HEADLINE_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--quick", action="store_true", help="headline workload only")
+    ap.add_argument("--fp8", action="store_true",
+                    help="step the chosen workload with an E4M3 KV cache")
     ap.add_argument("--cascade", action="store_true",
                     help="step the chosen workload through pa_attention_cascade (its shared "
                          "prefix as the common prefix; the prefix-sharing workload has one)")

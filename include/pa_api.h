@@ -155,6 +155,44 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 KV cache ("vLLM: An Exhaustive Technical Study for Kernel Engineers",
+ * 2.8 Quantization & compute kernels: --kv-cache-dtype fp8 stores K and V as
+ * E4M3 with one fp32 scale per tensor, k_scale and v_scale; FP8 halves the
+ * bytes of a block). E4M3 here is the OCP 8-bit format the GPU implements:
+ * 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities, largest
+ * finite 448.
+ *
+ * pa_write_kv_fp8: as pa_write_kv, but the caches hold one byte per element
+ * ([num_blocks][num_kv_heads][block_size][head_dim] uint8) and each element
+ * is stored as E4M3(x / scale): the quotient is a correctly rounded binary32
+ * division, the conversion rounds to nearest even and saturates at +-448.
+ * k_scale / v_scale must be finite and > 0 (PA_ERR_INVALID_ARG otherwise).
+ */
+pa_status pa_write_kv_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                          void* k_cache, void* v_cache, float k_scale, float v_scale,
+                          int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, void* stream);
+
+/*
+ * pa_attention_fp8: pa_attention over E4M3 caches written by pa_write_kv_fp8.
+ * Keys are value(code) * k_scale and values value(code) * v_scale; the
+ * dequantisation is fused into the split-KV kernel (codes widen exactly to
+ * fp32; k_scale is folded into the query scaling and v_scale into the output).
+ * Every span runs on the split-KV kernel: prefill chunks do not take the
+ * tensor-core path over an FP8 cache. The workspace is
+ * pa_attention_workspace_size(...) bytes, as for pa_attention. Errors as
+ * pa_attention, plus PA_ERR_INVALID_ARG for a scale that is not finite and > 0.
+ */
+pa_status pa_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, float scale, float k_scale,
+                           float v_scale, void* out, int num_reqs, int num_tokens,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, int max_blocks_per_req, int max_query_len,
+                           int max_seq_len, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
  * Cascade attention for a batch whose requests all share one common prefix
  * ("vLLM: An Exhaustive Technical Study for Kernel Engineers", 2.3 Automatic
  * prefix caching & KV reuse, cascade attention: when every request of a batch

@@ -67,6 +67,14 @@ def lib() -> ctypes.CDLL:
                                            _c_p, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i,
                                            _c_i, _c_i, _c_i, _c_p, ctypes.c_size_t, _c_p]
         L.pa_attention_cascade.restype = _c_i
+        L.pa_write_kv_fp8.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, ctypes.c_float,
+                                      ctypes.c_float, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p]
+        L.pa_write_kv_fp8.restype = _c_i
+        L.pa_attention_fp8.argtypes = [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, ctypes.c_float,
+                                       ctypes.c_float, ctypes.c_float, _c_p, _c_i, _c_i, _c_i,
+                                       _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_i, _c_p,
+                                       ctypes.c_size_t, _c_p]
+        L.pa_attention_fp8.restype = _c_i
         L.pa_status_string.argtypes = [_c_i]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_get_device_error.argtypes = [ctypes.POINTER(_c_i), ctypes.POINTER(ctypes.c_longlong),
@@ -167,6 +175,55 @@ def attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         int(max_query_len), int(max_seq_len), _dev(workspace, torch.uint8, "workspace"),
         int(workspace.numel()), _stream_ptr(stream))
     _check(st, "pa_attention")
+    return out
+
+
+def write_kv_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: float, v_scale: float,
+                 stream=None) -> None:
+    """pa_write_kv_fp8: quantise k/v [T, Hkv, D] bf16 into E4M3 caches
+    [num_blocks, Hkv, 16, D] (uint8) with per-tensor scales."""
+    T, hkv, d = k.shape
+    nb, hkv2, bs, d2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or hkv2 != hkv or d2 != d:
+        raise ValueError("shape mismatch between k/v and the caches")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [num_tokens]")
+    st = lib().pa_write_kv_fp8(_dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+                               _dev(slot_mapping, torch.int64, "slot_mapping"),
+                               _dev(k_cache, torch.uint8, "k_cache"),
+                               _dev(v_cache, torch.uint8, "v_cache"), float(k_scale),
+                               float(v_scale), T, hkv, d, bs, nb, _stream_ptr(stream))
+    _check(st, "pa_write_kv_fp8")
+
+
+def attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                  block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                  query_start_loc: torch.Tensor, scale: float, k_scale: float, v_scale: float,
+                  *, max_query_len: int, max_seq_len: int, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """pa_attention_fp8 over E4M3 caches (uint8 [num_blocks, Hkv, 16, D])."""
+    T, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    R = int(seq_lens.shape[0])
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q and the caches")
+    if query_start_loc.shape != (R + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != R:
+        raise ValueError("metadata shapes must be qsl [R+1], block_tables [R, max_blocks]")
+    if out is None:
+        out = torch.empty_like(q)
+    need = workspace_size(R, T, hq, hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().pa_attention_fp8(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.uint8, "k_cache"),
+        _dev(v_cache, torch.uint8, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
+        _dev(seq_lens, torch.int32, "seq_lens"),
+        _dev(query_start_loc, torch.int32, "query_start_loc"), float(scale), float(k_scale),
+        float(v_scale), _dev(out, torch.bfloat16, "out"), R, T, hq, hkv, d, bs, nb,
+        int(block_tables.shape[1]), int(max_query_len), int(max_seq_len),
+        _dev(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream_ptr(stream))
+    _check(st, "pa_attention_fp8")
     return out
 
 

@@ -46,8 +46,9 @@ constexpr unsigned kFull = 0xffffffffu;
 // =============================================================================
 // Split-KV decode kernel
 // =============================================================================
-template <int D, int G>
+template <int D, int G, bool F8>
 struct Cfg {
+  static constexpr int EB = F8 ? 1 : 2;          // bytes per cached K/V element
   static constexpr int DPT = (G <= 4) ? 16 : 8;  // q.k dims per lane
   static constexpr int TPT = D / DPT;            // lanes per token in q.k
   static constexpr int TPP = 32 / TPT;           // tokens per q.k pass
@@ -55,7 +56,7 @@ struct Cfg {
   static constexpr int LOG_G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   static constexpr int LPR = D / 4;   // lanes per V row (4 dims each)
   static constexpr int RPS = 32 / LPR;  // V rows per step
-  static constexpr int KV_BYTES = kBlockSize * D * 2;
+  static constexpr int KV_BYTES = kBlockSize * D * EB;
   static constexpr int Q_BYTES = G * D * 2;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES + Q_BYTES;
   static constexpr int P_BYTES = kBlockSize * G * 4 + 64;  // p[16][G], alpha[G]
@@ -63,9 +64,9 @@ struct Cfg {
   static_assert(DPT == 8 || DPT == 16, "one or two 16-byte chunks per lane");
 };
 
-template <int D, int G, int NSTAGE>
+template <int D, int G, int NSTAGE, bool F8>
 struct WarpSmem {
-  using C = Cfg<D, G>;
+  using C = Cfg<D, G, F8>;
   static constexpr int RAW = NSTAGE * C::STAGE_BYTES + C::P_BYTES + NSTAGE * 8;
   static constexpr int BYTES = (RAW + 127) / 128 * 128;
 };
@@ -120,10 +121,10 @@ struct Loc {
   int k, tok, req, len, base;
 };
 
-template <int D, int G, int WARPS, int NSTAGE>
+template <int D, int G, int WARPS, int NSTAGE, bool F8>
 __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParams p) {
-  using C = Cfg<D, G>;
-  using WS = WarpSmem<D, G, NSTAGE>;
+  using C = Cfg<D, G, F8>;
+  using WS = WarpSmem<D, G, NSTAGE, F8>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* const wsm = smem + warp * WS::BYTES;  // this warp's region
@@ -223,11 +224,12 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     if (lane == 0) {
       const uint32_t dst = stage0 + stage * C::STAGE_BYTES;
       const uint32_t bar = bars + 8 * stage;
-      const size_t off = ((size_t)pid * Hkv + kv) * (kBlockSize * D);
+      const size_t off = ((size_t)pid * Hkv + kv) * (kBlockSize * D) * C::EB;  // bytes
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(bar, 2 * C::KV_BYTES + (with_q ? C::Q_BYTES : 0));
-      bulk_g2s(dst, p.k_cache + off, C::KV_BYTES, bar);
-      bulk_g2s(dst + C::KV_BYTES, p.v_cache + off, C::KV_BYTES, bar);
+      bulk_g2s(dst, static_cast<const unsigned char*>(p.k_cache) + off, C::KV_BYTES, bar);
+      bulk_g2s(dst + C::KV_BYTES, static_cast<const unsigned char*>(p.v_cache) + off, C::KV_BYTES,
+               bar);
       if (with_q)
         bulk_g2s(dst + 2 * C::KV_BYTES, p.q + ((size_t)tok * Hq + (size_t)kv * G) * D, C::Q_BYTES,
                  bar);
@@ -249,7 +251,9 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   // ---- per-lane roles ---------------------------------------------------------------
   const int sub = lane % C::TPT;                                 // q.k dim slice
   const int tg = lane / C::TPT;                                  // token within a pass
-  const int swz = (C::DPT == 16) ? ((lane >> 2) & 1) : 0;        // bank-conflict-free order
+  // bf16 rows: a lane's 32 bytes are two 16-byte chunks, read in an order
+  // that avoids bank conflicts; E4M3 rows: one chunk, natural order
+  const int swz = (!F8 && C::DPT == 16) ? ((lane >> 2) & 1) : 0;
   const int hsel = head_of_lane<G>(lane);
   const int rl = lane % C::LPR;                                  // V dims 4*rl .. 4*rl+3
   const int rrow = lane / C::LPR;                                // V row within a step
@@ -344,9 +348,25 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 #pragma unroll
     for (int ps = 0; ps < C::NPASS; ++ps) {
       const int t = ps * C::TPP + tg;
-      const unsigned char* const row = st_ptr + t * D * 2 + sub * C::DPT * 2;
+      const unsigned char* const row = st_ptr + t * D * C::EB + sub * C::DPT * C::EB;
       float2 kf[C::DPT / 2];
-      {
+      if constexpr (F8) {  // E4M3 codes, dequantised exactly (k_scale is folded into q)
+        if constexpr (C::DPT == 16) {
+          const uint4 a = *reinterpret_cast<const uint4*>(row);
+          const uint32_t wv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            kf[2 * i] = e4m3x2_to_float2((uint16_t)(wv[i] & 0xffffu));
+            kf[2 * i + 1] = e4m3x2_to_float2((uint16_t)(wv[i] >> 16));
+          }
+        } else {
+          const uint2 a = *reinterpret_cast<const uint2*>(row);
+          kf[0] = e4m3x2_to_float2((uint16_t)(a.x & 0xffffu));
+          kf[1] = e4m3x2_to_float2((uint16_t)(a.x >> 16));
+          kf[2] = e4m3x2_to_float2((uint16_t)(a.y & 0xffffu));
+          kf[3] = e4m3x2_to_float2((uint16_t)(a.y >> 16));
+        }
+      } else {
         const uint4 a = *reinterpret_cast<const uint4*>(row + 16 * swz);
         kf[0] = bf16x2_to_float2(a.x);
         kf[1] = bf16x2_to_float2(a.y);
@@ -412,15 +432,22 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
       // Keys past the sequence end have p = 0; their V rows (which may hold
       // anything, NaN included) are replaced by the last valid row so the
       // loop needs no per-token branch: 0 * finite adds nothing.
-      const unsigned char* const vbase = st_ptr + C::KV_BYTES + rl * 8;
+      const unsigned char* const vbase = st_ptr + C::KV_BYTES + rl * 4 * C::EB;
       const int tmax = nvalid - 1;
 #pragma unroll
       for (int stp = 0; stp < kBlockSize / C::RPS; ++stp) {
         const int t = stp * C::RPS + rrow;
         {
-          const uint2 vv = *reinterpret_cast<const uint2*>(vbase + min(t, tmax) * D * 2);
-          const float2 v01 = bf16x2_to_float2(vv.x);
-          const float2 v23 = bf16x2_to_float2(vv.y);
+          float2 v01, v23;
+          if constexpr (F8) {  // v_scale is applied to the output
+            const uint32_t vv = *reinterpret_cast<const uint32_t*>(vbase + min(t, tmax) * D);
+            v01 = e4m3x2_to_float2((uint16_t)(vv & 0xffffu));
+            v23 = e4m3x2_to_float2((uint16_t)(vv >> 16));
+          } else {
+            const uint2 vv = *reinterpret_cast<const uint2*>(vbase + min(t, tmax) * D * 2);
+            v01 = bf16x2_to_float2(vv.x);
+            v23 = bf16x2_to_float2(vv.y);
+          }
           float2 ph[G];
           if constexpr (G >= 4) {
 #pragma unroll
@@ -534,7 +561,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
           if (rrow == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              const float inv = 1.f / Ls[h];
+              const float inv = p.v_scale / Ls[h];
               uint2 pk;
               pk.x = float2_to_bf16x2(O[h].x * inv, O[h].y * inv);
               pk.y = float2_to_bf16x2(O[h].z * inv, O[h].w * inv);
@@ -544,7 +571,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
         } else if (rrow == 0) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float inv = 1.f / lh[h];
+            const float inv = p.v_scale / lh[h];
             uint2 pk;
             pk.x = float2_to_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
             pk.y = float2_to_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
@@ -606,7 +633,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
           if (rrow == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              const float inv = 1.f / Ls[h];
+              const float inv = p.v_scale / Ls[h];
               uint2 pk;
               pk.x = float2_to_bf16x2(O[h].x * inv, O[h].y * inv);
               pk.y = float2_to_bf16x2(O[h].z * inv, O[h].w * inv);
@@ -622,10 +649,10 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 // ---- launch ---------------------------------------------------------------------------
 // Grid of a split-KV launch on the current device: every SM filled to its
 // occupancy, capped so the workers fit the workspace's partial slots.
-template <int D, int G, int WARPS, int NSTAGE>
+template <int D, int G, int WARPS, int NSTAGE, bool F8>
 cudaError_t decode_grid(int num_sms, int occ_cap, int* grid_out) {
-  auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE>;
-  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE>::BYTES;
+  auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE, F8>;
+  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE, F8>::BYTES;
   static int occ_cache[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -646,12 +673,12 @@ cudaError_t decode_grid(int num_sms, int occ_cap, int* grid_out) {
   return cudaSuccess;
 }
 
-template <int D, int G, int WARPS, int NSTAGE>
+template <int D, int G, int WARPS, int NSTAGE, bool F8>
 cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s) {
-  auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE>;
-  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE>::BYTES;
+  auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE, F8>;
+  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE, F8>::BYTES;
   int grid = 0;
-  cudaError_t e = decode_grid<D, G, WARPS, NSTAGE>(num_sms, occ_cap, &grid);
+  cudaError_t e = decode_grid<D, G, WARPS, NSTAGE, F8>(num_sms, occ_cap, &grid);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -688,54 +715,68 @@ cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cud
 #define PA_DEC64_STAGES 3
 #endif
 
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
-                          int occ_cap, cudaStream_t s) {
-  constexpr int W128 = PA_DEC128_WARPS, S128 = PA_DEC128_STAGES;
-  constexpr int W128G8 = PA_DEC128G8_WARPS, S128G8 = PA_DEC128G8_STAGES;
-  constexpr int W64 = PA_DEC64_WARPS, S64 = PA_DEC64_STAGES;
-  if (head_dim == 128) {
-    switch (group) {
-      case 1: return launch_decode_t<128, 1, W128, S128>(p, num_sms, occ_cap, s);
-      case 2: return launch_decode_t<128, 2, W128, S128>(p, num_sms, occ_cap, s);
-      case 4: return launch_decode_t<128, 4, W128, S128>(p, num_sms, occ_cap, s);
-      case 8: return launch_decode_t<128, 8, W128G8, S128G8>(p, num_sms, occ_cap, s);
-    }
-  } else if (head_dim == 64) {
-    switch (group) {
-      case 1: return launch_decode_t<64, 1, W64, S64>(p, num_sms, occ_cap, s);
-      case 2: return launch_decode_t<64, 2, W64, S64>(p, num_sms, occ_cap, s);
-      case 4: return launch_decode_t<64, 4, W64, S64>(p, num_sms, occ_cap, s);
-      case 8: return launch_decode_t<64, 8, W64, S64>(p, num_sms, occ_cap, s);
-    }
-  }
-  return cudaErrorInvalidValue;
+#ifndef PA_DEC128F8_STAGES
+#define PA_DEC128F8_STAGES 3
+#endif
+#ifndef PA_DEC64F8_STAGES
+#define PA_DEC64F8_STAGES 3
+#endif
+
+// Warps per CTA and ring stages per warp of each instantiation. An E4M3 tile
+// is half the bytes of a bf16 one: three-stage FP8 rings leave room for three
+// CTAs per SM (the FP8 calls run three; measured: the stage count itself
+// hardly matters, the extra warps do).
+template <int D, int G, bool F8>
+struct Tuning {
+  static constexpr int WARPS =
+      D == 128 ? (G == 8 ? PA_DEC128G8_WARPS : PA_DEC128_WARPS) : PA_DEC64_WARPS;
+  static constexpr int STAGES =
+      F8 ? (D == 128 ? PA_DEC128F8_STAGES : PA_DEC64F8_STAGES)
+         : (D == 128 ? (G == 8 ? PA_DEC128G8_STAGES : PA_DEC128_STAGES) : PA_DEC64_STAGES);
+};
+
+template <int D, int G, bool F8>
+cudaError_t launch_one(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s) {
+  using T = Tuning<D, G, F8>;
+  return launch_decode_t<D, G, T::WARPS, T::STAGES, F8>(p, num_sms, occ_cap, s);
 }
 
-}  // namespace pa
-
-namespace pa {
-int decode_workers(int head_dim, int group, int num_sms, int occ_cap) {
+template <int D, int G, bool F8>
+int workers_one(int num_sms, int occ_cap) {
+  using T = Tuning<D, G, F8>;
   int grid = 0;
-  cudaError_t e = cudaErrorInvalidValue;
-  constexpr int W128 = PA_DEC128_WARPS, S128 = PA_DEC128_STAGES;
-  constexpr int W128G8 = PA_DEC128G8_WARPS, S128G8 = PA_DEC128G8_STAGES;
-  constexpr int W64 = PA_DEC64_WARPS, S64 = PA_DEC64_STAGES;
-  int warps = 0;
-  if (head_dim == 128) {
-    switch (group) {
-      case 1: e = decode_grid<128, 1, W128, S128>(num_sms, occ_cap, &grid); warps = W128; break;
-      case 2: e = decode_grid<128, 2, W128, S128>(num_sms, occ_cap, &grid); warps = W128; break;
-      case 4: e = decode_grid<128, 4, W128, S128>(num_sms, occ_cap, &grid); warps = W128; break;
-      case 8: e = decode_grid<128, 8, W128G8, S128G8>(num_sms, occ_cap, &grid); warps = W128G8; break;
-    }
-  } else if (head_dim == 64) {
-    switch (group) {
-      case 1: e = decode_grid<64, 1, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
-      case 2: e = decode_grid<64, 2, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
-      case 4: e = decode_grid<64, 4, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
-      case 8: e = decode_grid<64, 8, W64, S64>(num_sms, occ_cap, &grid); warps = W64; break;
-    }
-  }
-  return e == cudaSuccess ? grid * warps : 0;
+  if (decode_grid<D, G, T::WARPS, T::STAGES, F8>(num_sms, occ_cap, &grid) != cudaSuccess) return 0;
+  return grid * T::WARPS;
 }
+
+// Calls FN<D, G, F8>(args...) for the runtime (head_dim, group, f8).
+#define PA_DECODE_DISPATCH(FN, FAIL, ...)                                             \
+  do {                                                                                \
+    if (head_dim == 128) {                                                            \
+      switch (group) {                                                                \
+        case 1: return f8 ? FN<128, 1, true>(__VA_ARGS__) : FN<128, 1, false>(__VA_ARGS__); \
+        case 2: return f8 ? FN<128, 2, true>(__VA_ARGS__) : FN<128, 2, false>(__VA_ARGS__); \
+        case 4: return f8 ? FN<128, 4, true>(__VA_ARGS__) : FN<128, 4, false>(__VA_ARGS__); \
+        case 8: return f8 ? FN<128, 8, true>(__VA_ARGS__) : FN<128, 8, false>(__VA_ARGS__); \
+      }                                                                               \
+    } else if (head_dim == 64) {                                                      \
+      switch (group) {                                                                \
+        case 1: return f8 ? FN<64, 1, true>(__VA_ARGS__) : FN<64, 1, false>(__VA_ARGS__);   \
+        case 2: return f8 ? FN<64, 2, true>(__VA_ARGS__) : FN<64, 2, false>(__VA_ARGS__);   \
+        case 4: return f8 ? FN<64, 4, true>(__VA_ARGS__) : FN<64, 4, false>(__VA_ARGS__);   \
+        case 8: return f8 ? FN<64, 8, true>(__VA_ARGS__) : FN<64, 8, false>(__VA_ARGS__);   \
+      }                                                                               \
+    }                                                                                 \
+    return FAIL;                                                                      \
+  } while (0)
+
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool f8, int num_sms,
+                          int occ_cap, cudaStream_t s) {
+  PA_DECODE_DISPATCH(launch_one, cudaErrorInvalidValue, p, num_sms, occ_cap, s);
+}
+
+int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap) {
+  PA_DECODE_DISPATCH(workers_one, 0, num_sms, occ_cap);
+}
+
 }  // namespace pa

@@ -4,6 +4,7 @@
 // Validation happens before any CUDA call, so a malformed call is rejected
 // without touching (or needing) a GPU.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -100,10 +101,17 @@ pa_status pa_init(void) {
   return device_state(&d);
 }
 
-pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache,
-                      void* v_cache, int num_tokens, int num_kv_heads, int head_dim,
-                      int block_size, int num_blocks, void* stream) {
+}  // extern "C"
+
+namespace {
+
+pa_status write_kv_impl(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache,
+                        void* v_cache, int kv_fp8, float k_scale, float v_scale, int num_tokens,
+                        int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                        void* stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0)
+    return PA_ERR_INVALID_ARG;
+  if (kv_fp8 && !(k_scale > 0.f && k_scale < INFINITY && v_scale > 0.f && v_scale < INFINITY))
     return PA_ERR_INVALID_ARG;
   if (block_size != kBlockSize || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PA_OK;
@@ -117,8 +125,11 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
   p.k = static_cast<const uint16_t*>(k);
   p.v = static_cast<const uint16_t*>(v);
   p.slot_mapping = slot_mapping;
-  p.k_cache = static_cast<uint16_t*>(k_cache);
-  p.v_cache = static_cast<uint16_t*>(v_cache);
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.kv_fp8 = kv_fp8;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
   p.num_tokens = num_tokens;
   p.num_kv_heads = num_kv_heads;
   p.head_dim = head_dim;
@@ -129,6 +140,25 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
   const cudaError_t e = launch_write_kv(p, s);
   g_launches.fetch_add(1);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping, void* k_cache,
+                      void* v_cache, int num_tokens, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, void* stream) {
+  return write_kv_impl(k, v, slot_mapping, k_cache, v_cache, 0, 1.f, 1.f, num_tokens,
+                       num_kv_heads, head_dim, block_size, num_blocks, stream);
+}
+
+pa_status pa_write_kv_fp8(const void* k, const void* v, const int64_t* slot_mapping,
+                          void* k_cache, void* v_cache, float k_scale, float v_scale,
+                          int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                          int num_blocks, void* stream) {
+  return write_kv_impl(k, v, slot_mapping, k_cache, v_cache, 1, k_scale, v_scale, num_tokens,
+                       num_kv_heads, head_dim, block_size, num_blocks, stream);
 }
 
 size_t pa_attention_workspace_size(int num_reqs, int num_tokens, int num_q_heads,
@@ -157,8 +187,12 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
                          const int32_t* query_start_loc, float scale, void* out, int num_reqs,
                          int num_tokens, int num_q_heads, int num_kv_heads, int head_dim,
                          int block_size, int num_blocks, int max_blocks_per_req,
-                         int max_query_len, int max_seq_len, int prefix_len, void* workspace,
+                         int max_query_len, int max_seq_len, int prefix_len, int kv_fp8,
+                         float k_scale, float v_scale, void* workspace,
                          size_t workspace_bytes, void* stream) {
+  if (kv_fp8 && !(k_scale > 0.f && k_scale < INFINITY && v_scale > 0.f && v_scale < INFINITY))
+    return PA_ERR_INVALID_ARG;
+  if (kv_fp8 && prefix_len > 0) return PA_ERR_UNSUPPORTED;  // no FP8 cascade
   if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       head_dim <= 0 || num_blocks < 0 || max_blocks_per_req < 0 || max_query_len < 0 ||
       max_seq_len < 0)
@@ -221,10 +255,12 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   pp.max_query_len = max_query_len;
   pp.max_seq_len = max_seq_len;
   pp.group = group;
-  // a cascade sends every span to the split-KV path
-  pp.use_prefill = (prefix_len == 0 && max_query_len >= kPrefillMinQlen) ? 1 : 0;
-  const int occ_cap = prefix_len > 0 ? PA_DEC_OCC_CAP_CASCADE : PA_DEC_OCC_CAP;
-  pp.num_workers = decode_workers(head_dim, pp.group, d->num_sms, occ_cap);
+  // a cascade, and an E4M3 cache (the tile kernel takes bf16 K/V), send every
+  // span to the split-KV path
+  pp.use_prefill = (prefix_len == 0 && !kv_fp8 && max_query_len >= kPrefillMinQlen) ? 1 : 0;
+  const int occ_cap =
+      prefix_len > 0 ? PA_DEC_OCC_CAP_CASCADE : (kv_fp8 ? PA_DEC_OCC_CAP_FP8 : PA_DEC_OCC_CAP);
+  pp.num_workers = decode_workers(head_dim, pp.group, kv_fp8 != 0, d->num_sms, occ_cap);
   if (pp.num_workers <= 0) return PA_ERR_CUDA;
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
   pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
@@ -271,15 +307,17 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
 
   DecodeParams dp;
   dp.q = static_cast<const uint16_t*>(q);
-  dp.k_cache = static_cast<const uint16_t*>(k_cache);
-  dp.v_cache = static_cast<const uint16_t*>(v_cache);
+  dp.k_cache = k_cache;
+  dp.v_cache = v_cache;
+  dp.v_scale = kv_fp8 ? v_scale : 1.f;
   dp.block_tables = block_tables;
   dp.out = static_cast<uint16_t*>(out);
   dp.bt_stride = max_blocks_per_req;
   dp.num_q_heads = num_q_heads;
   dp.num_kv_heads = num_kv_heads;
   dp.num_blocks = num_blocks;
-  dp.scale_log2 = scale * 1.4426950408889634f;
+  // scores in base-2 units; an E4M3 cache's k_scale rides on q
+  dp.scale_log2 = scale * 1.4426950408889634f * (kv_fp8 ? k_scale : 1.f);
   dp.header = pp.header;
   dp.units = pp.units;
   dp.worker_unit = num_tokens <= kPlanSmemTokens ? pp.worker_unit : nullptr;
@@ -294,7 +332,8 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   {
     TimerScope timer(2, s);
     const cudaError_t e =
-        launch_decode(dp, head_dim, num_q_heads / num_kv_heads, d->num_sms, occ_cap, s);
+        launch_decode(dp, head_dim, num_q_heads / num_kv_heads, kv_fp8 != 0, d->num_sms, occ_cap,
+                      s);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
@@ -314,8 +353,22 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        size_t workspace_bytes, void* stream) {
   return attention_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out,
                         num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
-                        num_blocks, max_blocks_per_req, max_query_len, max_seq_len, 0, workspace,
-                        workspace_bytes, stream);
+                        num_blocks, max_blocks_per_req, max_query_len, max_seq_len, 0, 0, 1.f,
+                        1.f, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           const int32_t* query_start_loc, float scale, float k_scale,
+                           float v_scale, void* out, int num_reqs, int num_tokens,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, int max_blocks_per_req, int max_query_len,
+                           int max_seq_len, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  return attention_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out,
+                        num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, max_blocks_per_req, max_query_len, max_seq_len, 0, 1,
+                        k_scale, v_scale, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_attention_cascade(const void* q, const void* k_cache, const void* v_cache,
@@ -330,7 +383,7 @@ pa_status pa_attention_cascade(const void* q, const void* k_cache, const void* v
   return attention_impl(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out,
                         num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
                         num_blocks, max_blocks_per_req, max_query_len, max_seq_len,
-                        common_prefix_len, workspace, workspace_bytes, stream);
+                        common_prefix_len, 0, 1.f, 1.f, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_get_device_error(int* code, long long* detail, int clear) {

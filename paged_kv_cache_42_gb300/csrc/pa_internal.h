@@ -166,8 +166,9 @@ struct PrefillLaunch {
 
 struct DecodeParams {
   const uint16_t* q;
-  const uint16_t* k_cache;
-  const uint16_t* v_cache;
+  const void* k_cache;  // bf16, or E4M3 codes in the f8 instantiation
+  const void* v_cache;
+  float v_scale;        // output multiplier: the E4M3 V scale, 1 for bf16
   const int32_t* block_tables;
   uint16_t* out;
   int bt_stride, num_q_heads, num_kv_heads, num_blocks;
@@ -189,8 +190,10 @@ struct WriteParams {
   const uint16_t* k;
   const uint16_t* v;
   const int64_t* slot_mapping;
-  uint16_t* k_cache;
-  uint16_t* v_cache;
+  void* k_cache;  // bf16, or E4M3 codes when kv_fp8
+  void* v_cache;
+  int kv_fp8;
+  float k_scale, v_scale;  // E4M3 caches only
   int num_tokens, num_kv_heads, head_dim;
   long long num_slots;
   unsigned long long* err;
@@ -208,10 +211,11 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 // head_dim / G select the instantiation; unsupported combinations return
 // cudaErrorInvalidValue. occ_cap bounds the resident CTAs per SM (the grid is
 // SMs x min(occupancy, occ_cap)).
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, int num_sms,
+// f8 selects the E4M3-cache instantiation.
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool f8, int num_sms,
                           int occ_cap, cudaStream_t s);
 // Split-KV workers launch_decode will use on this device (0 on error).
-int decode_workers(int head_dim, int group, int num_sms, int occ_cap);
+int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap);
 
 // Resident split-KV CTAs per SM: two suit long per-token key ranges (each
 // worker's slice stays long); the short suffixes of a cascade call run better
@@ -221,6 +225,9 @@ int decode_workers(int head_dim, int group, int num_sms, int occ_cap);
 #endif
 #ifndef PA_DEC_OCC_CAP_CASCADE
 #define PA_DEC_OCC_CAP_CASCADE 3
+#endif
+#ifndef PA_DEC_OCC_CAP_FP8
+#define PA_DEC_OCC_CAP_FP8 3  // E4M3 calls: smaller rings, a third CTA per SM
 #endif
 cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s);
 

@@ -141,6 +141,26 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
   return r;
 }
 
+// E4M3 (OCP 8-bit float: bias 7, no infinities, max 448) conversions.
+// Two binary32 values to two E4M3 codes, rounding to nearest even and
+// saturating to +-448 (cvt.rn.satfinite); `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two E4M3 codes (low byte first) to two binary32 values, exactly (through
+// f16x2, which holds every E4M3 value).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t w) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(w));
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, u;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return make_float2(lo, hi);
+}
+
 // 2^x with the hardware approximation (PTX ex2.approx.ftz.f32): one MUFU op,
 // relative error ~2^-22, results below 2^-126 flushed to zero.
 __device__ __forceinline__ float ex2_approx(float x) {
