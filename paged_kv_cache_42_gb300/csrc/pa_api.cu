@@ -255,9 +255,8 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   pp.max_query_len = max_query_len;
   pp.max_seq_len = max_seq_len;
   pp.group = group;
-  // a cascade, and an E4M3 cache (the tile kernel takes bf16 K/V), send every
-  // span to the split-KV path
-  pp.use_prefill = (prefix_len == 0 && !kv_fp8 && max_query_len >= kPrefillMinQlen) ? 1 : 0;
+  // a cascade sends every span to the split-KV path
+  pp.use_prefill = (prefix_len == 0 && max_query_len >= kPrefillMinQlen) ? 1 : 0;
   const int occ_cap =
       prefix_len > 0 ? PA_DEC_OCC_CAP_CASCADE : (kv_fp8 ? PA_DEC_OCC_CAP_FP8 : PA_DEC_OCC_CAP);
   pp.num_workers = decode_workers(head_dim, pp.group, kv_fp8 != 0, d->num_sms, occ_cap);
@@ -282,6 +281,8 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
     pl.prefix_chunks = chunks;
     pl.slot_floats = lay.slot_floats;
     pl.prefix_partials = prefix_partials;
+    pl.kv_fp8 = kv_fp8;
+    pl.v_scale = kv_fp8 ? v_scale : 1.f;
     pl.q = q;
     pl.k_cache = k_cache;
     pl.v_cache = v_cache;
@@ -297,7 +298,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
     pl.head_dim = head_dim;
     pl.num_blocks = num_blocks;
     pl.bt_stride = max_blocks_per_req;
-    pl.scale_log2 = scale * 1.4426950408889634f;
+    pl.scale_log2 = scale * 1.4426950408889634f * (kv_fp8 ? k_scale : 1.f);
     pl.err = d->err;
     TimerScope timer(prefix_len > 0 ? 4 : 3, s);
     const cudaError_t e = launch_prefill(pl, d->num_sms, s);

@@ -150,6 +150,10 @@ struct PrefillLaunch {
   // output is fp32 partials, one slot per (chunk, token, kv head)
   int prefix_len, prefix_chunks, slot_floats;
   float* prefix_partials;
+  // E4M3 caches: k_cache / v_cache hold codes; k_scale is already folded into
+  // scale_log2, v_scale multiplies the output
+  int kv_fp8;
+  float v_scale;
   const void* q;
   const void* k_cache;
   const void* v_cache;

@@ -38,6 +38,14 @@
 // max, sum, unnormalised output) per (chunk, token, kv head) for the split-KV
 // kernel to merge, instead of bf16 rows.
 //
+// FP8 caches (the F8 instantiation; "vLLM: An Exhaustive Technical Study for
+// Kernel Engineers", 2.8: E4M3 codes with per-tensor k_scale / v_scale): four
+// more warps (448 threads) load each key tile's E4M3 rows with plain
+// coalesced loads (one thread per key row) and widen them to bf16 - exactly,
+// every E4M3 value being a bf16 - straight into the 128B-swizzled operand
+// layout the MMA reads, then arrive on the stage's full barrier. k_scale is
+// folded into the softmax scale and v_scale into the epilogue.
+//
 // Warp roles (320 threads): warp 0 issues TMA loads (both Q tiles per work
 // item, K into a 3-stage ring released right after both S MMAs of a key tile,
 // V into a 2-stage ring released after both P*V), warp 1 allocates TMEM and
@@ -89,7 +97,8 @@ enum : int {
   B_COUNT = 21
 };
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;     // bf16 caches
+constexpr int kThreadsF8 = 448;   // E4M3 caches: + 4 converter warps
 
 }  // namespace
 
@@ -108,6 +117,10 @@ struct PrefillParams {
   // cascade prefix pass
   int num_tokens, prefix_len, prefix_chunks, prefix_pairs, slot_floats;
   float* prefix_partials;
+  // E4M3 caches (F8): raw codes and the output multiplier (1 for bf16)
+  const unsigned char* k_cache8;
+  const unsigned char* v_cache8;
+  float v_scale;
   unsigned long long* err;
 };
 
@@ -152,8 +165,41 @@ __device__ __forceinline__ Item get_item(const PrefillParams& p, int t) {
   return it;
 }
 
-template <int D, int G, bool PREFIX>
-__global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_constant__ PrefillParams p) {
+// One key row of an E4M3 tile widened to bf16 into a 128B-swizzled operand
+// tile (row r: 16-byte unit u of 64-element chunk c lives at
+// c * CHUNK + r * 128 + (u ^ (r & 7)) * 16). A row that is not a key of the
+// sequence is written as zeros.
+template <int D>
+__device__ __forceinline__ void widen_e4m3_row(const unsigned char* src, bool valid,
+                                               unsigned char* tile, int r) {
+  constexpr int CHUNK = 128 * 128;
+  uint4 raw[D / 16];
+#pragma unroll
+  for (int j = 0; j < D / 16; ++j)
+    raw[j] = valid ? __ldg(reinterpret_cast<const uint4*>(src) + j) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int j = 0; j < D / 16; ++j) {
+    const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = e4m3x2_to_float2((uint16_t)(w4[i] & 0xffffu));
+      const float2 b = e4m3x2_to_float2((uint16_t)(w4[i] >> 16));
+      o[2 * i] = float2_to_bf16x2(a.x, a.y);
+      o[2 * i + 1] = float2_to_bf16x2(b.x, b.y);
+    }
+    // elements 16j .. 16j+15: chunk 16j / 64, units (16j % 64) / 8 and the next
+    const int c = (16 * j) / 64, u = ((16 * j) % 64) / 8;
+    unsigned char* const rowp = tile + c * CHUNK + r * 128;
+    *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(rowp + (((u + 1) ^ (r & 7)) << 4)) =
+        make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <int D, int G, bool PREFIX, bool F8>
+__global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
+    pa_prefill_kernel(const __grid_constant__ PrefillParams p) {
   using C = PCfg<D, G>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -169,7 +215,11 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
       // every other slot once, by an expect_tx arrive or an MMA commit.
       const bool by_threads = (i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_EMPTY ||
                                i == B_O_EMPTY + 1);
-      mbar_init(bar0 + 8 * i, by_threads ? 128 : 1);
+      // E4M3 caches: the K / V stages are filled by the 4 converter warps
+      const bool by_converters =
+          F8 && ((i >= B_K_FULL && i < B_K_FULL + C::KSTAGES) ||
+                 (i >= B_V_FULL && i < B_V_FULL + C::VSTAGES));
+      mbar_init(bar0 + 8 * i, by_threads ? 128 : (by_converters ? 4 : 1));
     }
     fence_barrier_init();
   }
@@ -227,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
             tma_load_3d(base + C::OFF_Q + rt * C::Q_BYTES + c * C::CHUNK, &p.tm_q, c * 64,
                         tl.kv * G, tl.tok0 + rt * C::TOK, BAR(B_Q_FULL));
       }
-      for (int i = 0; i < tl.n; ++i, ++g) {
+      for (int i = 0; !F8 && i < tl.n; ++i, ++g) {  // E4M3: the converter warps load K/V
         if (i > 0 && (i & 3) == 0) {
           pid_cur = pid_nxt;
           pid_nxt = (i + 4 < tl.n) ? load_group((i >> 2) + 1) : -1;
@@ -307,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         if (rt == 0) {
           if (!wait(B_V_FULL + vst, (gv / C::VSTAGES) & 1)) return false;
           const int kv0 = (tl.i0 + i) * 128;
-          if (kv0 + 128 > L) {
+          if (!F8 && kv0 + 128 > L) {  // (the converters write such rows as zeros)
             // Rows of keys past the sequence end may hold anything (NaN too);
             // their P is 0, but 0 * NaN would poison O, so clear them.
             const int r0 = L - kv0;
@@ -354,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
     if (lane == 0) umma_commit(BAR(B_DRAIN));
     __syncwarp();
     mbar_wait_bounded(BAR(B_DRAIN), 0);
-  } else {
+  } else if (warp < 10) {
     // ======================= softmax + epilogue (warpgroup rt: warps 2-5, 6-9) ==========
     const int rt = (warp - 2) >> 2;  // row tile of this warpgroup
     const int q4 = warp & 3;         // TMEM lane quarter this warp may access
@@ -496,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
         mbar_arrive(BAR(B_O_EMPTY + rt));
         continue;
       }
-      const float inv = 1.f / l;
+      const float inv = p.v_scale / l;
       const bool store = j < qlen;
       uint16_t* const orow =
           p.out + ((size_t)(tl.tok0 - tl.j0 + j) * p.num_q_heads + (size_t)tl.kv * G + (m % G)) * D;
@@ -519,6 +569,40 @@ __global__ void __launch_bounds__(kThreads, 1) pa_prefill_kernel(const __grid_co
       }
       tc_fence_before();
       mbar_arrive(BAR(B_O_EMPTY + rt));
+    }
+  } else if constexpr (F8) {
+    // ======================= E4M3 converters (warps 10-13) =======================
+    const int r = threadIdx.x - kThreads;  // key row of the tile, 0..127
+    int g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+      const Item tl = get_item<D, G, PREFIX>(p, t);
+      const int32_t* const bt_row = p.block_tables + (size_t)tl.req * p.bt_stride;
+      for (int i = 0; i < tl.n; ++i, ++g) {
+        const int key = (tl.i0 + i) * 128 + r;
+        bool valid = key < tl.L;
+        size_t src = 0;
+        if (valid) {
+          const int pid = __ldg(bt_row + key / kBlockSize);
+          if (pid < 0 || pid >= p.num_blocks) {
+            report_error(p.err, PA_DEVERR_BLOCK_ID, key / kBlockSize);
+            valid = false;
+          } else {
+            src = (((size_t)pid * p.num_kv_heads + tl.kv) * kBlockSize + (key % kBlockSize)) * D;
+          }
+        }
+        const int ks = g % C::KSTAGES, vs = g % C::VSTAGES;
+        if (g >= C::KSTAGES && !wait(B_K_EMPTY + ks, ((g / C::KSTAGES) - 1) & 1)) { ok = false; break; }
+        widen_e4m3_row<D>(p.k_cache8 + src, valid, gbase + C::OFF_K + ks * C::KV_BYTES, r);
+        fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_K_FULL + ks));
+        if (g >= C::VSTAGES && !wait(B_V_EMPTY + vs, ((g / C::VSTAGES) - 1) & 1)) { ok = false; break; }
+        widen_e4m3_row<D>(p.v_cache8 + src, valid, gbase + C::OFF_V + vs * C::KV_BYTES, r);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_V_FULL + vs));
+      }
     }
   }
 
@@ -567,7 +651,7 @@ bool encode_bf16(CUtensorMap* m, int rank, const void* ptr, const cuuint64_t* di
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int G, bool PREFIX>
+template <int D, int G, bool PREFIX, bool F8>
 cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
   using C = PCfg<D, G>;
   PrefillParams p;
@@ -577,7 +661,7 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
     const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)C::TOK};
     if (!encode_bf16(&p.tm_q, 3, a.q, dims, str, box)) return cudaErrorInvalidValue;
   }
-  {
+  if (!F8) {  // E4M3 K/V are loaded by the converter warps, not by TMA
     const cuuint64_t rows = (cuuint64_t)a.num_blocks * a.num_kv_heads * kBlockSize;
     const cuuint64_t dims[2] = {(cuuint64_t)D, rows};
     const cuuint64_t str[1] = {(cuuint64_t)D * 2};
@@ -603,13 +687,16 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
   p.prefix_pairs = prefix_pairs(a.num_tokens, G);
   p.slot_floats = a.slot_floats;
   p.prefix_partials = a.prefix_partials;
+  p.k_cache8 = F8 ? static_cast<const unsigned char*>(a.k_cache) : nullptr;
+  p.v_cache8 = F8 ? static_cast<const unsigned char*>(a.v_cache) : nullptr;
+  p.v_scale = F8 ? a.v_scale : 1.f;
   int grid = num_sms;
   if (PREFIX) {
     const int items = p.prefix_pairs * a.num_kv_heads * a.prefix_chunks;
     grid = items < num_sms ? items : num_sms;
   }
 
-  auto kern = pa_prefill_kernel<D, G, PREFIX>;
+  auto kern = pa_prefill_kernel<D, G, PREFIX, F8>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -621,7 +708,7 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(F8 ? kThreadsF8 : kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -634,22 +721,22 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
 
 }  // namespace
 
-template <bool PREFIX>
+template <bool PREFIX, bool F8>
 cudaError_t launch_prefill_mode(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
   const int G = a.num_q_heads / a.num_kv_heads;
   if (a.head_dim == 128) {
     switch (G) {
-      case 1: return launch_prefill_t<128, 1, PREFIX>(a, num_sms, s);
-      case 2: return launch_prefill_t<128, 2, PREFIX>(a, num_sms, s);
-      case 4: return launch_prefill_t<128, 4, PREFIX>(a, num_sms, s);
-      case 8: return launch_prefill_t<128, 8, PREFIX>(a, num_sms, s);
+      case 1: return launch_prefill_t<128, 1, PREFIX, F8>(a, num_sms, s);
+      case 2: return launch_prefill_t<128, 2, PREFIX, F8>(a, num_sms, s);
+      case 4: return launch_prefill_t<128, 4, PREFIX, F8>(a, num_sms, s);
+      case 8: return launch_prefill_t<128, 8, PREFIX, F8>(a, num_sms, s);
     }
   } else if (a.head_dim == 64) {
     switch (G) {
-      case 1: return launch_prefill_t<64, 1, PREFIX>(a, num_sms, s);
-      case 2: return launch_prefill_t<64, 2, PREFIX>(a, num_sms, s);
-      case 4: return launch_prefill_t<64, 4, PREFIX>(a, num_sms, s);
-      case 8: return launch_prefill_t<64, 8, PREFIX>(a, num_sms, s);
+      case 1: return launch_prefill_t<64, 1, PREFIX, F8>(a, num_sms, s);
+      case 2: return launch_prefill_t<64, 2, PREFIX, F8>(a, num_sms, s);
+      case 4: return launch_prefill_t<64, 4, PREFIX, F8>(a, num_sms, s);
+      case 8: return launch_prefill_t<64, 8, PREFIX, F8>(a, num_sms, s);
     }
   }
   return cudaErrorInvalidValue;
@@ -657,8 +744,12 @@ cudaError_t launch_prefill_mode(const PrefillLaunch& a, int num_sms, cudaStream_
 
 cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
   if (!get_encoder()) return cudaErrorNotSupported;
-  return a.prefix_len > 0 ? launch_prefill_mode<true>(a, num_sms, s)
-                          : launch_prefill_mode<false>(a, num_sms, s);
+  if (a.kv_fp8) {
+    if (a.prefix_len > 0) return cudaErrorNotSupported;  // no FP8 cascade
+    return launch_prefill_mode<false, true>(a, num_sms, s);
+  }
+  return a.prefix_len > 0 ? launch_prefill_mode<true, false>(a, num_sms, s)
+                          : launch_prefill_mode<false, false>(a, num_sms, s);
 }
 
 }  // namespace pa

@@ -120,8 +120,10 @@ SWEEP = [
     ([8, 55, 16, 32, 200, 1000], [1] * 6, 4, 4, 64),
     ([100, 300, 17], [1, 1, 1], 32, 8, 128),
     ([50, 700, 2000], [1, 1, 1], 64, 8, 128),   # G 8
-    ([90, 0, 400], [1, 40, 3], 16, 8, 64),       # G 2, a 40-token chunk on the split-KV path
+    ([90, 0, 400], [1, 40, 3], 16, 8, 64),       # G 2, a 40-token chunk
     ([0, 513], [100, 1], 32, 8, 128),            # a long chunk with no context
+    ([300, 1000], [64, 37], 64, 8, 128),         # G 8 chunks on the tensor cores
+    ([200, 5], [130, 16], 8, 8, 64),             # MHA, D 64, ragged key tiles
 ]
 
 
