@@ -197,6 +197,15 @@ __device__ __forceinline__ void widen_e4m3_row(const unsigned char* src, bool va
   }
 }
 
+// The r-th work item of this CTA. Items come sorted longest first; rounds of
+// gridDim.x items alternate direction (CTA b takes b, then 2g-1-b, then
+// 2g+b, ...), so a CTA that drew a long item in one round draws a short one
+// in the next instead of the next-longest.
+__device__ __forceinline__ int snake_item(int r) {
+  const int g = (int)gridDim.x, b = (int)blockIdx.x;
+  return r * g + ((r & 1) ? g - 1 - b : b);
+}
+
 template <int D, int G, bool PREFIX, bool F8>
 __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     pa_prefill_kernel(const __grid_constant__ PrefillParams p) {
@@ -251,7 +260,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     // lanes 0..7 each copy one 16-key block.
     int g = 0, it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
+    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int nb = (tl.L + kBlockSize - 1) / kBlockSize;
       const int32_t* const bt_row = p.block_tables + (size_t)tl.req * p.bt_stride;
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     int np[2] = {0, 0};  // P_t events consumed
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
+    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int L = tl.L;
       if (!wait(B_Q_FULL, it & 1)) { ok = false; break; }
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     const uint32_t o_addr = trow + C::TM_O + 128 * rt;
     int ns = 0, it = 0;  // S_rt events consumed; work items done
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x, ++it) {
+    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int L = tl.L;
       int qlen = 0, j = 0, lim;
@@ -573,9 +582,9 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
   } else if constexpr (F8) {
     // ======================= E4M3 converters (warps 10-13) =======================
     const int r = threadIdx.x - kThreads;  // key row of the tile, 0..127
-    int g = 0;
+    int g = 0, it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < ntiles; t += gridDim.x) {
+    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int32_t* const bt_row = p.block_tables + (size_t)tl.req * p.bt_stride;
       for (int i = 0; i < tl.n; ++i, ++g) {
