@@ -68,6 +68,18 @@ namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
 
+// Threads per S row in the softmax (1 or 2). With 2, the two threads of a row
+// take 64 score columns each and combine their row maxima through shared
+// memory (a bounded mbarrier exchange). It shortens the softmax but not the
+// kernel: in steady state the tensor pipe, not the softmax, sets the pace of
+// a key tile (measured 52.6 us with 2 vs 51.4 us with 1 on the mixed batch),
+// so the default is 1.
+#ifndef PA_PREFILL_SPLIT
+#define PA_PREFILL_SPLIT 1
+#endif
+constexpr int kSplit = PA_PREFILL_SPLIT;
+static_assert(kSplit == 1 || kSplit == 2, "one or two threads per row");
+
 template <int D, int G>
 struct PCfg {
   static constexpr int TOK = 128 / G;         // chunk tokens per 128-row tile
@@ -75,18 +87,32 @@ struct PCfg {
   static constexpr int CHUNK = 128 * 128;     // one [128 rows][128 B] operand chunk
   static constexpr int Q_BYTES = NCH * CHUNK; // one row tile of Q
   static constexpr int KV_BYTES = NCH * CHUNK;  // one 128-key tile of K or of V
-  static constexpr int KSTAGES = 3;
+  // a third K stage does not fit beside the row-max exchange buffer
+#ifdef PA_PREFILL_KSTAGES
+  static constexpr int KSTAGES = PA_PREFILL_KSTAGES;
+#else
+  static constexpr int KSTAGES = kSplit == 2 ? 2 : 3;
+#endif
   static constexpr int VSTAGES = 2;
   static constexpr int OFF_Q = 0;  // two row tiles
   static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + KSTAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + VSTAGES * KV_BYTES;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + 1 KB alignment slack
+  // row-max / row-sum exchange of the split softmax: [row tile][parity][half][128 rows]
+  static constexpr int OFF_XCH = OFF_BAR + 256;
+  static constexpr int XCH_BYTES = kSplit == 2 ? 2 * 2 * 2 * 128 * 4 : 0;
+  static constexpr int SMEM = OFF_XCH + XCH_BYTES + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  // S_t (fp32, 128 columns) at 128*t; P_t (bf16 pairs, 64 columns) overwrites
-  // the first half of S_t; O_t at 256 + 128*t.
+  // S_t (fp32, 128 columns) at 128*t; P_t (bf16 pairs, 64 columns) is written
+  // over S_t, each thread's part over its own S columns (P column of key k:
+  // pcol(k / 32) + (k % 32) / 2); O_t at 256 + 128*t.
   static constexpr uint32_t TM_S = 0;
   static constexpr uint32_t TM_O = 256;
+  static constexpr int CPH = 4 / kSplit;  // 32-column S chunks per softmax thread
+  // first P column of S chunk c: chunk c's 32 scores become 16 bf16 pairs
+  __host__ __device__ static constexpr uint32_t pcol(int c) {
+    return 64u * (uint32_t)(c / CPH) + 16u * (uint32_t)(c % CPH);
+  }
 };
 
 // barrier slots
@@ -94,11 +120,13 @@ enum : int {
   B_Q_FULL = 0, B_Q_EMPTY = 1, B_K_FULL = 2 /* x3 */, B_K_EMPTY = 5 /* x3 */,
   B_V_FULL = 8 /* x2 */, B_V_EMPTY = 10 /* x2 */, B_S_FULL = 12 /* x2: per row tile */,
   B_P_FULL = 14 /* x2 */, B_PV_DONE = 16 /* x2 */, B_O_EMPTY = 18 /* x2 */, B_DRAIN = 20,
-  B_COUNT = 21
+  B_XCH = 21 /* x4: [row tile][parity], the split softmax's row exchange */,
+  B_COUNT = 25
 };
 
-constexpr int kThreads = 320;     // bf16 caches
-constexpr int kThreadsF8 = 448;   // E4M3 caches: + 4 converter warps
+constexpr int kSoftWarps = 8 * kSplit;            // 4 * split per row tile
+constexpr int kThreads = 32 * (2 + kSoftWarps);   // bf16 caches
+constexpr int kThreadsF8 = kThreads + 128;        // E4M3 caches: + 4 converter warps
 
 }  // namespace
 
@@ -223,12 +251,12 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
       // P_FULL and O_EMPTY are arrived at by the 128 threads of one warpgroup;
       // every other slot once, by an expect_tx arrive or an MMA commit.
       const bool by_threads = (i == B_P_FULL || i == B_P_FULL + 1 || i == B_O_EMPTY ||
-                               i == B_O_EMPTY + 1);
+                               i == B_O_EMPTY + 1 || (i >= B_XCH && i < B_XCH + 4));
       // E4M3 caches: the K / V stages are filled by the 4 converter warps
       const bool by_converters =
           F8 && ((i >= B_K_FULL && i < B_K_FULL + C::KSTAGES) ||
                  (i >= B_V_FULL && i < B_V_FULL + C::VSTAGES));
-      mbar_init(bar0 + 8 * i, by_threads ? 128 : (by_converters ? 4 : 1));
+      mbar_init(bar0 + 8 * i, by_threads ? 128 * kSplit : (by_converters ? 4 : 1));
     }
     fence_barrier_init();
   }
@@ -388,9 +416,9 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           const uint32_t a_tm = tmem + C::TM_S + 128 * rt;  // P_rt: 64 columns of bf16 pairs
           const uint64_t b0 = vmaj_base + ((C::OFF_V + vst * C::KV_BYTES) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ta(d, a_tm + 8 * ks, b0 + ((ks * 2048) >> 4), idesc_pv,
-                         (i > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks)  // keys 16 ks .. 16 ks + 15: 8 P columns
+            umma_bf16_ta(d, a_tm + C::pcol(ks >> 1) + 8 * (ks & 1), b0 + ((ks * 2048) >> 4),
+                         idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
           umma_commit(BAR(B_PV_DONE + rt));
           if (rt == 1) umma_commit(BAR(B_V_EMPTY + vst));
         }
@@ -413,14 +441,41 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     if (lane == 0) umma_commit(BAR(B_DRAIN));
     __syncwarp();
     mbar_wait_bounded(BAR(B_DRAIN), 0);
-  } else if (warp < 10) {
-    // ======================= softmax + epilogue (warpgroup rt: warps 2-5, 6-9) ==========
-    const int rt = (warp - 2) >> 2;  // row tile of this warpgroup
-    const int q4 = warp & 3;         // TMEM lane quarter this warp may access
-    const int m = q4 * 32 + lane;    // row == TMEM lane
+  } else if (warp < 2 + kSoftWarps) {
+    // ======================= softmax + epilogue ==========================================
+    // Row tile rt has warps 2 + 4*split*rt ...; within it, 4 warps per column
+    // half hf (warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31).
+    const int sw = warp - 2;
+    const int rt = sw / (4 * kSplit);     // row tile of this warp
+    const int hf = (sw / 4) % kSplit;     // column half (0 without the split)
+    const int q4 = warp & 3;              // TMEM lane quarter this warp may access
+    const int m = q4 * 32 + lane;         // row == TMEM lane
     const uint32_t trow = ((uint32_t)(q4 * 32) << 16) + tmem;
     const uint32_t s_addr = trow + C::TM_S + 128 * rt;
     const uint32_t o_addr = trow + C::TM_O + 128 * rt;
+    constexpr int OCH = D / 32 / kSplit;  // 32-column O chunks per thread
+    float* const xch = reinterpret_cast<float*>(gbase + C::OFF_XCH);
+    int nx = 0;  // exchanges done
+    // Combine a per-thread row value with the other half's (max or sum). The
+    // two halves meet on an mbarrier with a bounded wait (a half that gives up
+    // cannot strand the other); exchange k uses barrier and buffer k % 2, so
+    // a barrier is reused only after every thread has passed the other one.
+    auto exchange = [&](float v, bool take_max, bool& good) -> float {
+      if constexpr (kSplit == 1) {
+        return v;
+      } else {
+        const int k = nx++;
+        float* const xb = xch + ((rt * 2 + (k & 1)) * 2) * 128;
+        xb[hf * 128 + m] = v;
+        mbar_arrive(BAR(B_XCH + rt * 2 + (k & 1)));  // release: the store above is visible
+        if (!wait(B_XCH + rt * 2 + (k & 1), (k >> 1) & 1)) {
+          good = false;
+          return v;
+        }
+        const float o = xb[(1 - hf) * 128 + m];
+        return take_max ? fmaxf(v, o) : v + o;
+      }
+    };
     int ns = 0, it = 0;  // S_rt events consumed; work items done
     bool ok = true;
     for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
@@ -447,7 +502,8 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
         // pass 1: row max of the raw scores over visible keys
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < C::CPH; ++cc) {
+          const int c = hf * C::CPH + cc;
           uint32_t r[32];
           tmem_ld32(s_addr + c * 32, r);
           tmem_wait_ld();
@@ -460,6 +516,8 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
             for (int e = 0; e < 32; ++e) mx = fmaxf(mx, e <= lim_c ? __uint_as_float(r[e]) : -INFINITY);
           }
         }
+        mx = exchange(mx, true, ok);         // the whole row's max
+        if (!ok) break;
         const float mt = mx * p.scale_log2;  // -inf stays -inf
         float alpha = 1.f;
         bool resc = false;
@@ -472,7 +530,8 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
         }
         if (__any_sync(kAll, resc)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
+          for (int oc = 0; oc < OCH; ++oc) {
+            const int c = hf * OCH + oc;
             uint32_t o[32];
             tmem_ld32(o_addr + c * 32, o);
             tmem_wait_ld();
@@ -483,14 +542,15 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
           tmem_wait_st();
         }
         l *= alpha;
-        // pass 2: P = exp2(s * scale - m) as bf16 pairs, written over S: the 32
-        // S columns of chunk c become P columns 16c .. 16c+15, which only
-        // cover S columns already read.
+        // pass 2: P = exp2(s * scale - m) as bf16 pairs, written over this
+        // thread's own S columns: chunk c's 16 P columns start at pcol(c),
+        // which only covers S columns this thread has already read.
         const float nm = -m_used;
         const float sc = p.scale_log2;
         float l2[2] = {0.f, 0.f};  // two partial sums: shorter dependency chains
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int cc = 0; cc < C::CPH; ++cc) {
+          const int c = hf * C::CPH + cc;
           uint32_t r[32];
           tmem_ld32(s_addr + c * 32, r);
           tmem_wait_ld();
@@ -514,7 +574,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
               w[e] = float2_to_bf16x2(p0, p1);
             }
           }
-          tmem_st16(s_addr + 16 * c, w);
+          tmem_st16(s_addr + C::pcol(c), w);
         }
         l += l2[0] + l2[1];
         tmem_wait_st();
@@ -525,6 +585,8 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
       // ---- epilogue: O / l -> bf16 rows of out ----
       if (!wait(B_PV_DONE + rt, (ns - 1) & 1)) { ok = false; break; }
       tc_fence_after();
+      l = exchange(l, false, ok);  // the whole row's sum
+      if (!ok) break;
       if constexpr (PREFIX) {
         // fp32 partial of (chunk, token, kv head), head m % G of the slot
         const int tok = tl.tok0 + rt * C::TOK + m / G;
@@ -533,12 +595,13 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
         float* const slot = p.prefix_partials +
                             (((size_t)tl.chunk * p.num_tokens + (store ? tok : 0)) *
                                  p.num_kv_heads + tl.kv) * p.slot_floats;
-        if (store) {
+        if (store && hf == 0) {
           __stcg(slot + h, m_used);
           __stcg(slot + G + h, l);
         }
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int oc = 0; oc < OCH; ++oc) {
+          const int c = hf * OCH + oc;
           uint32_t o[32];
           tmem_ld32(o_addr + c * 32, o);
           tmem_wait_ld();
@@ -560,7 +623,8 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
       uint16_t* const orow =
           p.out + ((size_t)(tl.tok0 - tl.j0 + j) * p.num_q_heads + (size_t)tl.kv * G + (m % G)) * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int oc = 0; oc < OCH; ++oc) {
+        const int c = hf * OCH + oc;
         uint32_t o[32];
         tmem_ld32(o_addr + c * 32, o);
         tmem_wait_ld();
@@ -581,7 +645,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     }
   } else if constexpr (F8) {
     // ======================= E4M3 converters (warps 10-13) =======================
-    const int r = threadIdx.x - kThreads;  // key row of the tile, 0..127
+    const int r = threadIdx.x - kThreads;  // key row of the tile, 0..127 (converter warps)
     int g = 0, it = 0;
     bool ok = true;
     for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
