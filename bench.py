@@ -385,6 +385,37 @@ def fp8_timing(args, flush, torch, binding, dist, rank, world, peaks) -> dict:
             "requests_per_s": round(world * w.num_reqs / (ms * 1e-3), 1)}
 
 
+def graph_steps(res: Resident, steps: int, warmup: int, flush, torch, dist) -> float:
+    """ms per step when the step's calls (write + attention) are captured once
+    in a CUDA graph and replayed; the L2 flush stays outside the timed region."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        res.step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        res.step()
+    for _ in range(warmup):
+        flush()
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier(dist)
+    stream = torch.cuda.current_stream()
+    for i in range(steps):
+        flush()
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    del g
+    return max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, dist)
+
+
 def run_ours(args, rank, world, local, dist):
     import torch
 
@@ -427,6 +458,7 @@ def run_ours(args, rank, world, local, dist):
         pre_ms = max_over_ranks(t["prefill_ms"], dist)
         entry = {"w": w, "sb": sb, "t": t, "ms": ms, "dec_ms": dec_ms, "pre_ms": pre_ms,
                  "res": res, "steps": steps}
+        entry["graph_ms"] = graph_steps(res, steps, args.warmup, flush, torch, dist)
         if idx == args.config and not args.no_e2e:
             te = time_steps(res, max(20, steps // 4), args.warmup, flush, torch, binding, dist,
                             e2e=True)
@@ -468,6 +500,10 @@ def run_ours(args, rank, world, local, dist):
             "algorithmic_bytes_per_launch": sb["attention"],
             "kernel_ms": round(main["dec_ms"], 5)},
         "gpu_launches": int(main["t"]["launches"]),
+        "cuda_graph": {"ms_per_step": round(main["graph_ms"], 5),
+                       "value": round(world * sb["step"] / (main["graph_ms"] * 1e-3) / 1e9, 2),
+                       "unit": "GB/s",
+                       "what": "the same step's calls captured once in a CUDA graph and replayed"},
         "prefill_kernel_ms": round(main["pre_ms"], 5) if main["pre_ms"] > 0 else None,
         "clocks": main["t"]["clocks"],
     }
@@ -486,6 +522,8 @@ def run_ours(args, rank, world, local, dist):
             "workload": f"{wl.CONFIG_NAMES[MIXED_CONFIG]}: {wl.CONFIG_DESCRIPTIONS[MIXED_CONFIG]}",
             "value": round(world * mw.num_tokens / (m["ms"] * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(m["ms"], 5), "steps": m["steps"],
+            "cuda_graph_ms_per_step": round(m["graph_ms"], 5),
+            "cuda_graph_value": round(world * mw.num_tokens / (m["graph_ms"] * 1e-3), 1),
             "attention_kernel_ms": round(m["dec_ms"], 5),
             "prefill_kernel_ms": round(m["pre_ms"], 5),
             "prefill_tflops": round(prefill_flops(mw) / (m["pre_ms"] * 1e-3) / 1e12, 1)
