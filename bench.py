@@ -278,7 +278,12 @@ class Resident:
 
 
 def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, dist,
-               e2e: bool = False, clocks: ClockSampler | None = None):
+               e2e: bool = False, clocks: ClockSampler | None = None, timers: bool = False):
+    """Time `steps` steps (CUDA events on the launching stream, L2 flushed
+    before each). With timers, the library also records events around its
+    decode and tensor-core launches (kernel durations for the roofline); those
+    events serialise the chained launches, so the step time is taken from a
+    pass without them."""
     fn = res.step_e2e if e2e else res.step
     for _ in range(warmup):
         flush()
@@ -306,9 +311,10 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
     stream = torch.cuda.current_stream()
     for i in range(steps):
         flush()
-        binding.set_kernel_timer("decode", dk[i][0], dk[i][1])
-        if has_prefill:
-            binding.set_kernel_timer(pre_kernel, pk[i][0], pk[i][1])
+        if timers:
+            binding.set_kernel_timer("decode", dk[i][0], dk[i][1])
+            if has_prefill:
+                binding.set_kernel_timer(pre_kernel, pk[i][0], pk[i][1])
         ev[i][0].record(stream)
         fn()
         ev[i][1].record(stream)
@@ -319,11 +325,18 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
     clk = clocks.stop() if clocks else None
     barrier(dist)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    dec_ms = [a.elapsed_time(b) for a, b in dk]
-    pre_ms = [a.elapsed_time(b) for a, b in pk] if has_prefill else [0.0]
+    dec_ms = [a.elapsed_time(b) for a, b in dk] if timers else [0.0]
+    pre_ms = [a.elapsed_time(b) for a, b in pk] if (timers and has_prefill) else [0.0]
     return {"ms_per_step": sum(step_ms) / steps, "ms_median": statistics.median(step_ms),
-            "decode_ms": sum(dec_ms) / steps, "prefill_ms": sum(pre_ms) / len(pre_ms),
+            "decode_ms": sum(dec_ms) / len(dec_ms), "prefill_ms": sum(pre_ms) / len(pre_ms),
             "launches": launches, "clocks": clk}
+
+
+def time_kernels(res: Resident, steps: int, warmup: int, flush, torch, binding, dist) -> dict:
+    """Kernel durations (decode / tensor-core) from a separate timed pass."""
+    t = time_steps(res, steps, warmup, flush, torch, binding, dist, timers=True)
+    return {"decode_ms": max_over_ranks(t["decode_ms"], dist),
+            "prefill_ms": max_over_ranks(t["prefill_ms"], dist)}
 
 
 def prefix_share_timing(args, flush, torch, binding, dist, rank, world) -> dict:
@@ -339,12 +352,13 @@ def prefix_share_timing(args, flush, torch, binding, dist, rank, world) -> dict:
     for name, casc in (("plain", 0), ("cascade", w.shared_prefix_blocks * 16)):
         res = Resident(w, torch, binding, cascade_len=casc)
         t = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
+        tk = time_kernels(res, steps, args.warmup, flush, torch, binding, dist)
         code, detail = binding.get_device_error(clear=True)
         if code:
             raise RuntimeError(f"device error {code} at {detail}")
         ms = max_over_ranks(t["ms_per_step"], dist)
-        dec = max_over_ranks(t["decode_ms"], dist)
-        pre = max_over_ranks(t["prefill_ms"], dist) if casc else 0.0
+        dec = tk["decode_ms"]
+        pre = tk["prefill_ms"] if casc else 0.0
         attn_ms = dec + pre
         out[name] = {"ms_per_step": round(ms, 5), "decode_kernel_ms": round(dec, 5),
                      "tokens_per_s": round(world * w.num_tokens / (ms * 1e-3), 1),
@@ -368,11 +382,12 @@ def fp8_timing(args, flush, torch, binding, dist, rank, world, peaks) -> dict:
     steps = max(50, args.steps // 10)
     res = Resident(w, torch, binding, fp8_scales=FP8_SCALES)
     t = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
+    tk = time_kernels(res, steps, args.warmup, flush, torch, binding, dist)
     code, detail = binding.get_device_error(clear=True)
     if code:
         raise RuntimeError(f"device error {code} at {detail}")
     ms = max_over_ranks(t["ms_per_step"], dist)
-    dec = max_over_ranks(t["decode_ms"], dist)
+    dec = tk["decode_ms"]
     del res
     torch.cuda.empty_cache()
     achieved = attn8 / (dec * 1e-3) / 1e9
@@ -450,12 +465,13 @@ def run_ours(args, rank, world, local, dist):
         steps = args.steps if idx == args.config else max(50, args.steps // 10)
         t = time_steps(res, steps, args.warmup, flush, torch, binding, dist,
                        clocks=ClockSampler(local) if idx == args.config else None)
+        tk = time_kernels(res, steps, args.warmup, flush, torch, binding, dist)
         code, detail = binding.get_device_error(clear=True)
         if code:
             raise RuntimeError(f"device error {code} at {detail}")
         ms = max_over_ranks(t["ms_per_step"], dist)
-        dec_ms = max_over_ranks(t["decode_ms"], dist)
-        pre_ms = max_over_ranks(t["prefill_ms"], dist)
+        dec_ms = tk["decode_ms"]
+        pre_ms = tk["prefill_ms"]
         entry = {"w": w, "sb": sb, "t": t, "ms": ms, "dec_ms": dec_ms, "pre_ms": pre_ms,
                  "res": res, "steps": steps}
         entry["graph_ms"] = graph_steps(res, steps, args.warmup, flush, torch, dist)

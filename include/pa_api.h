@@ -291,6 +291,21 @@ pa_status pa_get_device_error(int* code, long long* detail, int clear);
  */
 pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event);
 
+/*
+ * Process-wide options.
+ *   PA_OPT_DECODE_SELF_PLAN (default 1): a batch whose spans are all at most
+ *     one token (pure decode), with at most 512 requests and no cascade, is
+ *     planned inside the split-KV kernel. That kernel then starts streaming
+ *     K/V without waiting for the planner or for the preceding KV write; it
+ *     waits for them (griddepcontrol.wait) only before reading a request's
+ *     last block, which holds the newest token, and before its first merge.
+ *     The results are bit-identical with the option off (the planner path),
+ *     which the tests compare. value 0 turns it off.
+ * PA_ERR_INVALID_ARG for an unknown option. Not thread-safe.
+ */
+#define PA_OPT_DECODE_SELF_PLAN 1
+pa_status pa_set_option(int option, int value);
+
 /* Number of kernel launches the library has issued in this process. */
 long long pa_launch_count(void);
 

@@ -281,6 +281,17 @@ def set_kernel_timer(kernel: str, start: torch.cuda.Event | None,
     _check(lib().pa_set_kernel_timer(KERNEL_IDS[kernel], sp, ep), "pa_set_kernel_timer")
 
 
+OPTIONS = {"decode_self_plan": 1}
+
+
+def set_option(name: str, value: int) -> None:
+    """pa_set_option: process-wide library options (see include/pa_api.h)."""
+    L = lib()
+    L.pa_set_option.argtypes = [_c_i, _c_i]
+    L.pa_set_option.restype = _c_i
+    _check(L.pa_set_option(OPTIONS[name], int(value)), "pa_set_option")
+
+
 def launch_count() -> int:
     return int(lib().pa_launch_count())
 

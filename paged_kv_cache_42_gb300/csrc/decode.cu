@@ -139,10 +139,60 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   }
   __syncwarp();
 
-  griddep_wait();  // the plan is written by the preceding grid
-
-  const int W = p.header->num_positions;
-  const int K = p.header->num_units;
+  // The work list: from the planner (the preceding grid), or - for a
+  // decode-only batch (every span at most one token) - built by this CTA from
+  // query_start_loc and seq_lens, without waiting for any earlier grid.
+  const UnitInfo* units = p.units;
+  int W, K;
+  bool waited = false;  // lane 0: griddepcontrol.wait done (plan, KV write visible)
+  if (p.self_plan) {
+    UnitInfo* const su = reinterpret_cast<UnitInfo*>(smem + WARPS * WS::BYTES);
+    __shared__ int s_tot[WARPS];
+    const int R = p.num_reqs, T = p.num_tokens, Hkv_ = p.num_kv_heads;
+    int carry = 0;
+    for (int r0 = 0; r0 < R; r0 += 32 * WARPS) {
+      const int r = r0 + warp * 32 + lane;
+      int n = 0, q0 = T, L = 0;
+      if (r < R) {
+        q0 = __ldg(p.qsl + r);
+        const int q1 = __ldg(p.qsl + r + 1);
+        L = __ldg(p.seq_lens + r);
+        const int qlen = q1 - q0;
+        if (q0 < 0 || q1 < q0 || q1 > T) {
+          report_error(p.err, PA_DEVERR_QSL, r);
+          q0 = T;
+        } else if (L < qlen || qlen > 1 || (L + kBlockSize - 1) / kBlockSize > p.max_blocks_per_req ||
+                   qlen > p.max_query_len || L > p.max_seq_len) {
+          report_error(p.err, PA_DEVERR_LENGTHS, r);
+        } else if (qlen == 1) {
+          n = Hkv_ * ((L + kBlockSize - 1) / kBlockSize);
+        }
+      }
+      int incl = n;  // warp inclusive scan of positions
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) s_tot[warp] = incl;
+      __syncthreads();
+      int off = carry;
+      for (int w2 = 0; w2 < warp; ++w2) off += s_tot[w2];
+      if (r < R) su[r] = UnitInfo{q0, r, L, off + incl - n};
+      for (int w2 = 0; w2 < WARPS; ++w2) carry += s_tot[w2];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) su[R] = UnitInfo{T, -1, 0, carry};
+    __syncthreads();
+    units = su;
+    W = carry;
+    K = R;
+  } else {
+    griddep_wait();  // the plan is written by the preceding grid
+    waited = true;
+    W = p.header->num_positions;
+    K = p.header->num_units;
+  }
   if (W <= 0) return;
   const int NW = plan_workers(W, gridDim.x * WARPS);
   const int w = blockIdx.x * WARPS + warp;
@@ -158,7 +208,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   // ---- batch metadata helpers ------------------------------------------------
   auto window = [&](int kbase) -> int {
     const int kk = kbase + lane;
-    return kk <= K ? __ldg(&p.units[kk].base) : 0x7fffffff;
+    return kk <= K ? units[kk].base : 0x7fffffff;
   };
   auto locate = [&](int y0, int kbase, int win) -> Loc {
     const int y = y0 + lane;
@@ -167,7 +217,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     for (int i = 0; i < 32; ++i) c += (__shfl_sync(kFull, win, i) <= y) ? 1 : 0;
     int k = kbase + c - 1;
     k = k < 0 ? 0 : (k > K ? K : k);
-    const int4 u = __ldg(reinterpret_cast<const int4*>(p.units) + k);
+    const int4 u = *reinterpret_cast<const int4*>(units + k);
     return Loc{k, u.x, u.y, u.z, u.w};
   };
   auto finish = [&](int y0, const Loc& kl) -> Batch {
@@ -199,7 +249,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   // ---- the unit holding the first position: from the planner, or a 32-ary
   // search over units[].base --------------------------------------------------------
   int lo = 0, hi = K;  // base[lo] <= S < base[hi]
-  if (p.worker_unit) {
+  if (p.worker_unit && !p.self_plan) {
     lo = __ldg(p.worker_unit + w);
     hi = lo + 1;
   }
@@ -207,7 +257,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   while (hi - lo > 1) {
     const int step = (hi - lo + 31) / 32;
     const int idx = lo + lane * step;
-    const bool ok = idx < hi && __ldg(&p.units[idx].base) <= S;
+    const bool ok = idx < hi && units[idx].base <= S;
     const unsigned bal = __ballot_sync(kFull, ok);
     const int last = 31 - __clz(bal);
     lo = lo + last * step;
@@ -220,8 +270,14 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   int nwin = 0, nkbase = 0;
   Loc nkl{0, 0, 0, 0, 0};
 
-  auto issue = [&](int stage, int pid, int kv, bool with_q, int tok) {
+  // last: the segment's last block, which holds the new token of a decode; in a
+  // self-planned launch its K/V come from the KV write, so wait for it first.
+  auto issue = [&](int stage, int pid, int kv, bool with_q, int tok, bool last) {
     if (lane == 0) {
+      if (last && !waited) {
+        griddep_wait();
+        waited = true;
+      }
       const uint32_t dst = stage0 + stage * C::STAGE_BYTES;
       const uint32_t bar = bars + 8 * stage;
       const size_t off = ((size_t)pid * Hkv + kv) * (kBlockSize * D) * C::EB;  // bytes
@@ -244,7 +300,8 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
       const int kv = __shfl_sync(kFull, cur.kv, i);
       const int blk = __shfl_sync(kFull, cur.blk, i);
       const int tok = __shfl_sync(kFull, cur.tok, i);
-      issue(i, pid, kv, i == 0 || blk == 0, tok);
+      const int nbi = __shfl_sync(kFull, cur.nb, i);
+      issue(i, pid, kv, i == 0 || blk == 0, tok, blk == nbi - 1);
     }
   }
 
@@ -480,19 +537,21 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
       const int yi = y + NSTAGE;
       if (yi < E) {
         const int ji = yi - y0;
-        int pid, kvi, blki, toki;
+        int pid, kvi, blki, toki, nbi;
         if (ji < 32) {
           pid = __shfl_sync(kFull, cur.pid, ji);
           kvi = __shfl_sync(kFull, cur.kv, ji);
           blki = __shfl_sync(kFull, cur.blk, ji);
           toki = __shfl_sync(kFull, cur.tok, ji);
+          nbi = __shfl_sync(kFull, cur.nb, ji);
         } else {
           pid = __shfl_sync(kFull, nxt.pid, ji - 32);
           kvi = __shfl_sync(kFull, nxt.kv, ji - 32);
           blki = __shfl_sync(kFull, nxt.blk, ji - 32);
           toki = __shfl_sync(kFull, nxt.tok, ji - 32);
+          nbi = __shfl_sync(kFull, nxt.nb, ji - 32);
         }
-        issue(stage, pid, kvi, blki == 0, toki);
+        issue(stage, pid, kvi, blki == 0, toki, blki == nbi - 1);
       }
     }
     if (++stage == NSTAGE) {
@@ -579,7 +638,9 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
           }
         }
       } else {
-        const int u = kk * Hkv + kv;
+        // merge slot and counter of this (token, kv head): tokens increase with
+        // the position order, so slot u + worker is unique per segment
+        const int u = tok * Hkv + kv;
         float* slot = p.partials + (size_t)(u + w) * p.slot_floats;
         if (lane == 0) {
 #pragma unroll
@@ -597,7 +658,13 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
         __threadfence();
         __syncwarp();
         int prev = 0;
-        if (lane == 0) prev = atomicAdd(p.counters + u, 1);
+        if (lane == 0) {
+          if (!waited) {  // the counters are zeroed by the planner
+            griddep_wait();
+            waited = true;
+          }
+          prev = atomicAdd(p.counters + u, 1);
+        }
         prev = __shfl_sync(kFull, prev, 0);
         if (prev == wl - wf) {  // every other segment has landed: merge them all
           __threadfence();
@@ -647,24 +714,34 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 }
 
 // ---- launch ---------------------------------------------------------------------------
+
 // Grid of a split-KV launch on the current device: every SM filled to its
 // occupancy, capped so the workers fit the workspace's partial slots.
+// Dynamic shared memory of a launch: the warps' rings, plus the unit table of
+// a self-planned launch.
 template <int D, int G, int WARPS, int NSTAGE, bool F8>
-cudaError_t decode_grid(int num_sms, int occ_cap, int* grid_out) {
+constexpr int decode_smem(bool self_plan) {
+  return WARPS * WarpSmem<D, G, NSTAGE, F8>::BYTES +
+         (self_plan ? (int)sizeof(UnitInfo) * (kSelfPlanMaxReqs + 1) : 0);
+}
+
+template <int D, int G, int WARPS, int NSTAGE, bool F8>
+cudaError_t decode_grid(int num_sms, int occ_cap, bool self_plan, int* grid_out) {
   auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE, F8>;
-  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE, F8>::BYTES;
-  static int occ_cache[64] = {0};
+  const int smem = decode_smem<D, G, WARPS, NSTAGE, F8>(self_plan);
+  static int occ_cache[64][2] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int occ = (dev >= 0 && dev < 64) ? occ_cache[dev] : 0;
+  int occ = (dev >= 0 && dev < 64) ? occ_cache[dev][self_plan] : 0;
   if (occ == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             decode_smem<D, G, WARPS, NSTAGE, F8>(true));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, WARPS * 32, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
-    if (dev >= 0 && dev < 64) occ_cache[dev] = occ;
+    if (dev >= 0 && dev < 64) occ_cache[dev][self_plan] = occ;
   }
   if (occ > occ_cap) occ = occ_cap;
   int grid = num_sms * occ;
@@ -676,9 +753,9 @@ cudaError_t decode_grid(int num_sms, int occ_cap, int* grid_out) {
 template <int D, int G, int WARPS, int NSTAGE, bool F8>
 cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s) {
   auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE, F8>;
-  constexpr int smem = WARPS * WarpSmem<D, G, NSTAGE, F8>::BYTES;
+  const int smem = decode_smem<D, G, WARPS, NSTAGE, F8>(p.self_plan != 0);
   int grid = 0;
-  cudaError_t e = decode_grid<D, G, WARPS, NSTAGE, F8>(num_sms, occ_cap, &grid);
+  cudaError_t e = decode_grid<D, G, WARPS, NSTAGE, F8>(num_sms, occ_cap, p.self_plan != 0, &grid);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -689,6 +766,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cud
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+  // Programmatic launch: the grid starts when the preceding grid triggers
+  // (the planner at its top for a self-planned batch, otherwise at its end).
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
@@ -745,7 +824,8 @@ template <int D, int G, bool F8>
 int workers_one(int num_sms, int occ_cap) {
   using T = Tuning<D, G, F8>;
   int grid = 0;
-  if (decode_grid<D, G, T::WARPS, T::STAGES, F8>(num_sms, occ_cap, &grid) != cudaSuccess) return 0;
+  if (decode_grid<D, G, T::WARPS, T::STAGES, F8>(num_sms, occ_cap, false, &grid) != cudaSuccess)
+    return 0;
   return grid * T::WARPS;
 }
 

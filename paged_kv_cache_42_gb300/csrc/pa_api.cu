@@ -32,6 +32,7 @@ struct DeviceState {
 std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<long long> g_launches{0};
+std::atomic<int> g_self_plan{1};  // pa_set_option(PA_OPT_DECODE_SELF_PLAN, ...)
 constexpr int kNumTimers = 5;  // write, plan, decode, prefill, cascade prefix
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
@@ -248,6 +249,12 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   pp.seq_lens = seq_lens;
   pp.block_tables = block_tables;
   pp.prefix_blocks = prefix_len / kBlockSize;
+  // a decode-only batch (every span at most one token) plans itself inside
+  // the split-KV kernel, which then overlaps the planner and the KV write
+  const int self_plan = (g_self_plan.load() && prefix_len == 0 && max_query_len <= 1 &&
+                         num_reqs <= kSelfPlanMaxReqs) ? 1 : 0;
+  pp.self_plan = self_plan;
+  pp.early_trigger = (self_plan || prefix_len > 0) ? 1 : 0;
   pp.num_reqs = num_reqs;
   pp.num_tokens = num_tokens;
   pp.num_kv_heads = num_kv_heads;
@@ -329,6 +336,13 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   dp.prefix_partials = prefix_partials;
   dp.prefix_chunks = chunks;
   dp.num_tokens = num_tokens;
+  dp.self_plan = self_plan;
+  dp.num_reqs = num_reqs;
+  dp.max_blocks_per_req = max_blocks_per_req;
+  dp.max_query_len = max_query_len;
+  dp.max_seq_len = max_seq_len;
+  dp.qsl = query_start_loc;
+  dp.seq_lens = seq_lens;
   dp.err = d->err;
   {
     TimerScope timer(2, s);
@@ -399,6 +413,15 @@ pa_status pa_get_device_error(int* code, long long* detail, int clear) {
     if (cudaMemcpy(d->err, z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
+}
+
+pa_status pa_set_option(int option, int value) {
+  switch (option) {
+    case PA_OPT_DECODE_SELF_PLAN:
+      g_self_plan.store(value ? 1 : 0);
+      return PA_OK;
+  }
+  return PA_ERR_INVALID_ARG;
 }
 
 pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event) {

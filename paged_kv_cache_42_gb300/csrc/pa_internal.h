@@ -16,6 +16,10 @@ constexpr int kBlockSize = 16;
 constexpr int kMaxDecodeWorkers = 4096;
 // The planner keeps per-token scratch in shared memory up to this many tokens.
 constexpr int kPlanSmemTokens = 4096;
+// A decode-only batch (every span at most one token) of up to this many
+// requests is planned by the split-KV kernel itself, in shared memory, so
+// that kernel need not wait for the planner or the KV write before streaming.
+constexpr int kSelfPlanMaxReqs = 512;
 
 // Split-KV workers used for W flattened positions when `all` are launched:
 // at least PA_DEC_MIN_POS positions each (the planner and the split-KV kernel
@@ -131,6 +135,9 @@ struct PlanParams {
   const int32_t* seq_lens;
   const int32_t* block_tables;  // read only for the cascade prefix check
   int prefix_blocks;            // cascade: blocks of the common prefix; 0 otherwise
+  int self_plan;                // decode-only batch planned by the split-KV kernel: only
+                                // zero the merge counters
+  int early_trigger;            // release the next grid at the top (it needs no plan at first)
   int num_reqs, num_tokens, num_kv_heads, max_blocks_per_req, max_query_len, max_seq_len;
   int group;        // G = Hq / Hkv
   int use_prefill;  // route requests with qlen >= kPrefillMinQlen to the tensor-core kernel
@@ -187,6 +194,10 @@ struct DecodeParams {
   int key_start_blocks;          // 0 without a cascade
   const float* prefix_partials;  // null without a cascade
   int prefix_chunks, num_tokens;
+  // self-planned decode-only batch: the kernel builds its unit table from these
+  int self_plan, num_reqs, max_blocks_per_req, max_query_len, max_seq_len;
+  const int32_t* qsl;
+  const int32_t* seq_lens;
   unsigned long long* err;
 };
 

@@ -53,9 +53,11 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 constexpr int kTileBuckets = 512;  // tiles sorted by key-tile count, longest first
 
 __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
-  // The dependent grid may be scheduled now; it waits for this grid to
-  // finish before reading the plan.
-  griddep_launch_dependents();
+  // When the next grid has work that needs no plan (a self-planned split-KV
+  // grid, the cascade prefix pass), let it start now; a grid that would only
+  // wait at its top for the plan is released at the end of this one instead
+  // (starting it early measured slower).
+  if (p.early_trigger) griddep_launch_dependents();
   __shared__ long long scan_sm[32];
   __shared__ int bucket_cnt[kTileBuckets];
   __shared__ int bucket_pos[kTileBuckets];
@@ -64,12 +66,27 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   // workspace.
   extern __shared__ int2 dsm[];
   const int T = p.num_tokens;
+  if (p.self_plan) {
+    // a decode-only batch plans itself in the split-KV kernel; that kernel
+    // only needs its merge counters zeroed, before its first merge
+    for (long long i = threadIdx.x; i < (long long)T * p.num_kv_heads; i += blockDim.x)
+      p.counters[i] = 0;
+    if (threadIdx.x == 0) {
+      p.header->num_units = 0;
+      p.header->num_positions = 0;
+      p.header->num_tiles = 0;
+    }
+    if (!p.early_trigger) griddep_launch_dependents();
+    griddep_wait();  // complete only after the KV write (see the end of this kernel)
+    return;
+  }
   const bool in_smem = T <= kPlanSmemTokens;
   int2* const raw = in_smem ? dsm : p.raw;
   int* const ubase = in_smem ? reinterpret_cast<int*>(dsm + T) : nullptr;
   // a prefill work item is a pair of 128-row tiles: 2 * 128 / G chunk tokens
   const int tok_per_item = 2 * (128 / p.group);
-  for (int b = threadIdx.x; b < kTileBuckets; b += blockDim.x) bucket_cnt[b] = 0;
+  if (p.use_prefill)
+    for (int b = threadIdx.x; b < kTileBuckets; b += blockDim.x) bucket_cnt[b] = 0;
   for (int t = threadIdx.x; t < T; t += blockDim.x) raw[t] = make_int2(-1, 0);
   __syncthreads();
 
@@ -116,13 +133,15 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     for (int j = 0; j < qlen; ++j) raw[q0 + j] = make_int2(r, ctx + j + 1);
   }
   __syncthreads();
-  {  // positions of the buckets, longest tiles first (exclusive scan, descending)
+  if (p.use_prefill) {  // positions of the buckets, longest tiles first (exclusive scan, descending)
     static_assert(kTileBuckets <= kPlanThreads, "one bucket per thread");
-    const int b = kTileBuckets - 1 - (int)threadIdx.x;
+    const int b = kTileBuckets - 1 - (int)threadIdx.x;  // blockDim is kPlanThreads here
     long long total;
     const long long ex = block_exclusive_scan(b >= 0 ? bucket_cnt[b] : 0, &total, scan_sm);
     if (b >= 0) bucket_pos[b] = (int)ex;
     if (threadIdx.x == 0) p.header->num_tiles = (int)total;
+  } else if (threadIdx.x == 0) {
+    p.header->num_tiles = 0;
   }
   __syncthreads();
   if (p.use_prefill) {
@@ -164,7 +183,8 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     p.header->num_units = K;
     p.header->num_positions = W;
   }
-  for (long long i = threadIdx.x; i < run_k * p.num_kv_heads; i += blockDim.x) p.counters[i] = 0;
+  for (long long i = threadIdx.x; i < (long long)T * p.num_kv_heads; i += blockDim.x)
+    p.counters[i] = 0;  // merge counters are per (token, kv head)
   // each split-KV worker's first unit (same worker count and slicing as the
   // split-KV kernel), found by binary search over the units' first positions
   if (ubase) {
@@ -183,6 +203,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   // Let the grid before this one (the KV write on the same stream) finish
   // before this grid completes: whoever waits on the plan then also sees the
   // newly written K/V.
+  if (!p.early_trigger) griddep_launch_dependents();
   griddep_wait();
 }
 
@@ -205,7 +226,16 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   // before completing.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(kPlanThreads);
+  // A batch with no tensor-core work needs no bucket sort: a block sized to the
+  // batch (fewer warps per barrier) plans it faster.
+  int threads = kPlanThreads;
+  if (p.self_plan) {
+    threads = 256;
+  } else if (!p.use_prefill) {
+    const int need = p.num_tokens > p.num_reqs ? p.num_tokens : p.num_reqs;
+    threads = need <= 128 ? 128 : need <= 256 ? 256 : need <= 512 ? 512 : kPlanThreads;
+  }
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

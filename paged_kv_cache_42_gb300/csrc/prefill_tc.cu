@@ -680,9 +680,11 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
   }
 
   if constexpr (PREFIX) {
-    // The split-KV grid launched after this one may start; this grid does not
-    // complete before the planner (and the KV write before it) has, so a
-    // dependent that waits for this grid sees the plan too.
+    // The split-KV grid launched after this one may start now; this grid does
+    // not complete before the planner (and the KV write before it) has, so a
+    // dependent that waits for this grid sees the plan too. (The prefill-chunk
+    // grid releases its dependent only by completing: triggering here too
+    // measured 0.53 vs 0.435 ms per mixed step.)
     griddep_launch_dependents();
     griddep_wait();
   }

@@ -237,3 +237,57 @@ def test_batch_larger_than_planner_shared_memory():
                          head_dim=64, seed=612, pool_factor=1.1)
     assert w.num_tokens > 4096
     _run_and_compare(w, "T > 4096", reqs=[0, 1, 2047, 4096, R - 3, R - 2, R - 1])
+
+
+# ---------------------------------------------------------------------------
+# self-planned decode-only batches against the planner path
+# ---------------------------------------------------------------------------
+def _decode_batches():
+    rng = np.random.default_rng(77)
+    yield "config 1", wl.make_config(1)
+    yield "config 2", wl.make_config(2)
+    yield "config 4", wl.make_config(4)
+    ctx = rng.integers(0, 3000, size=300)
+    ql = (rng.random(300) < 0.9).astype(np.int64)  # some requests have no new token
+    yield "300 requests, some idle", wl.make_workload(ctx, ql, num_q_heads=32, num_kv_heads=8,
+                                                     head_dim=128, seed=801, pool_factor=1.05)
+    yield "G 8, D 64", wl.make_workload(rng.integers(0, 900, size=40), [1] * 40, num_q_heads=16,
+                                        num_kv_heads=2, head_dim=64, seed=802)
+
+
+@pytest.mark.parametrize("which", range(5))
+def test_self_planned_decode_is_bit_identical_to_planner_path(which):
+    name, w = list(_decode_batches())[which]
+    b = gu.DeviceBatch(w)
+    b.write()
+    try:
+        binding.set_option("decode_self_plan", 1)
+        own = gu.to_bits(b.attend(out=torch.empty_like(b.q)))
+        binding.set_option("decode_self_plan", 0)
+        planned = gu.to_bits(b.attend(out=torch.empty_like(b.q)))
+    finally:
+        binding.set_option("decode_self_plan", 1)
+    torch.cuda.synchronize()
+    gu.check_no_device_error()
+    assert np.array_equal(own, planned), name
+    if w.num_tokens <= 400:
+        got = gu.to_f64(b.attend())
+        gu.assert_close(got[gu.rows_of(w, range(w.num_reqs))],
+                        gu.oracle_reference(w)[gu.rows_of(w, range(w.num_reqs))], name)
+
+
+def test_self_planned_decode_reports_bad_requests():
+    w = wl.make_workload([40, 20, 70], [1, 1, 1], num_q_heads=8, num_kv_heads=2, head_dim=128,
+                         seed=803)
+    b = gu.DeviceBatch(w)
+    b.write()
+    sl = w.seq_lens.copy()
+    sl[1] = w.max_seq_len + 5  # longer than the bound the call was given
+    b.seq_lens = torch.from_numpy(sl).cuda()
+    out = b.attend()
+    torch.cuda.synchronize()
+    code, detail = binding.get_device_error(clear=True)
+    assert code == 3 and detail == 1
+    assert torch.isnan(out[1].float()).all()
+    ref = gu.oracle_reference(wl.subset_requests(w, [0, 2]))
+    gu.assert_close(gu.to_f64(out[[0, 2]]), ref, "good requests next to a bad one")
