@@ -218,6 +218,7 @@ class Resident:
         self.binding = binding
         self.cascade_len = cascade_len  # > 0: attention through pa_attention_cascade
         self.fp8 = fp8_scales           # (k_scale, v_scale): an E4M3 cache
+        self.signature = workload_signature(w)  # the NVTX range name of a step
         dev = torch.device("cuda")
 
         def bf(bits):
@@ -291,6 +292,20 @@ class Resident:
         self.h_out.copy_(self.out, non_blocking=True)
 
 
+def workload_signature(w: wl.Workload) -> str:
+    """The step's profile name, execute_context_A(a)_generation_B(b). A
+    synthetic batch has no prompts, so a request with more than one query
+    token counts as a prefill chunk (context) and a one-token query as a
+    decode (generation)."""
+    from paged_kv_cache_42_gb300 import host
+
+    ql = np.diff(np.asarray(w.query_start_loc, dtype=np.int64))
+    ctx = ql > 1
+    return host.step_signature({
+        "num_context_reqs": int(ctx.sum()), "num_context_tokens": int(ql[ctx].sum()),
+        "num_generation_reqs": int((~ctx).sum()), "num_generation_tokens": int(ql[~ctx].sum())})
+
+
 def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, dist,
                e2e: bool = False, clocks: ClockSampler | None = None, timers: bool = False):
     """Time `steps` steps (CUDA events on the launching stream, L2 flushed
@@ -323,6 +338,7 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
         time.sleep(0.3)
     n0 = binding.launch_count()
     stream = torch.cuda.current_stream()
+    nvtx = torch.cuda.nvtx
     for i in range(steps):
         flush()
         if timers:
@@ -330,7 +346,9 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
             if has_prefill:
                 binding.set_kernel_timer(pre_kernel, pk[i][0], pk[i][1])
         ev[i][0].record(stream)
+        nvtx.range_push(res.signature)
         fn()
+        nvtx.range_pop()
         ev[i][1].record(stream)
     binding.set_kernel_timer("decode", None, None)
     binding.set_kernel_timer(pre_kernel, None, None)
@@ -487,7 +505,7 @@ def run_ours(args, rank, world, local, dist):
         dec_ms = tk["decode_ms"]
         pre_ms = tk["prefill_ms"]
         entry = {"w": w, "sb": sb, "t": t, "ms": ms, "dec_ms": dec_ms, "pre_ms": pre_ms,
-                 "res": res, "steps": steps}
+                 "res": res, "steps": steps, "signature": res.signature}
         entry["graph_ms"] = graph_steps(res, steps, args.warmup, flush, torch, dist)
         if idx == args.config and not args.no_e2e:
             te = time_steps(res, max(20, steps // 4), args.warmup, flush, torch, binding, dist,
@@ -520,6 +538,7 @@ def run_ours(args, rank, world, local, dist):
         "config": {"workload": f"{wl.CONFIG_NAMES[args.config]}: "
                                f"{wl.CONFIG_DESCRIPTIONS[args.config]}",
                    "num_reqs": w.num_reqs, "num_tokens": w.num_tokens,
+                   "step_signature": main["signature"],
                    "l2": "flushed before every timed step (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {
@@ -552,6 +571,7 @@ def run_ours(args, rank, world, local, dist):
             "workload": f"{wl.CONFIG_NAMES[MIXED_CONFIG]}: {wl.CONFIG_DESCRIPTIONS[MIXED_CONFIG]}",
             "value": round(world * mw.num_tokens / (m["ms"] * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(m["ms"], 5), "steps": m["steps"],
+            "step_signature": m["signature"],
             "cuda_graph_ms_per_step": round(m["graph_ms"], 5),
             "cuda_graph_value": round(world * mw.num_tokens / (m["graph_ms"] * 1e-3), 1),
             "attention_kernel_ms": round(m["dec_ms"], 5),

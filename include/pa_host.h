@@ -178,6 +178,13 @@ typedef struct pa_sched_output {
   int max_query_len, max_seq_len;
   int block_table_stride;   /* row stride of block_tables, >= 1 */
   int num_decode_reqs;      /* requests granted 1 token that is past their prompt */
+  /* The step's profile signature ("vLLM v1 Deep Dive: How LLM(...) and the
+   * Server Boot and Generate", Part 3, Step 4c: a trace names each forward
+   * execute_context_A(a)_generation_B(b)): context requests are those whose
+   * span starts inside their prompt (prefill, chunked or not), generation
+   * requests those whose span starts past it (decode); with their tokens. */
+  int num_context_reqs, num_context_tokens;
+  int num_generation_reqs, num_generation_tokens;
 } pa_sched_output;
 
 /* A scheduler drawing blocks from `pool`, which it does not own and which

@@ -284,7 +284,9 @@ class Scheduler:
         # the batch the kernels take
         out = dict(req_ids=[], num_scheduled=[], num_computed=[], query_start_loc=[0],
                    seq_lens=[], block_tables=[], slot_mapping=[], positions=[],
-                   input_tokens=[], preempted_ids=preempted, num_decode_reqs=0)
+                   input_tokens=[], preempted_ids=preempted, num_decode_reqs=0,
+                   num_context_reqs=0, num_context_tokens=0, num_generation_reqs=0,
+                   num_generation_tokens=0)
         width = max([len(r.blocks) for r, _ in scheduled] + [1])  # widest scheduled request
         for r, n in scheduled:
             ctx = r.num_computed
@@ -300,6 +302,11 @@ class Scheduler:
                 out["slot_mapping"].append(r.blocks[p // bs] * bs + p % bs)
             if n == 1 and ctx >= r.prompt_len:
                 out["num_decode_reqs"] += 1
+            # the step's profile signature ("vLLM v1 Deep Dive", Part 3, Step 4c):
+            # a span that starts inside the prompt is context, otherwise generation
+            phase = "context" if ctx < r.prompt_len else "generation"
+            out[f"num_{phase}_reqs"] += 1
+            out[f"num_{phase}_tokens"] += n
         out["num_tokens"] = out["query_start_loc"][-1]
         out["max_query_len"] = max(out["num_scheduled"], default=0)
         out["max_seq_len"] = max(out["seq_lens"], default=0)

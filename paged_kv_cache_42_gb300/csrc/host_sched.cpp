@@ -243,6 +243,7 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
   int stride = 1;
   for (auto& e : sched) stride = std::max(stride, (int)e.first->blocks.size());
   int t = 0, max_q = 0, max_s = 0, decodes = 0;
+  int ctx_reqs = 0, ctx_toks = 0, gen_reqs = 0, gen_toks = 0;
   for (size_t k = 0; k < sched.size(); ++k) {
     Req* r = sched[k].first;
     const int n = sched[k].second, ctx = r->num_computed;
@@ -265,6 +266,13 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
     max_q = std::max(max_q, n);
     max_s = std::max(max_s, ctx + n);
     decodes += (n == 1 && ctx >= r->prompt_len);
+    if (ctx < r->prompt_len) {
+      ++ctx_reqs;
+      ctx_toks += n;
+    } else {
+      ++gen_reqs;
+      gen_toks += n;
+    }
   }
   out->query_start_loc[sched.size()] = t;
   out->num_reqs = (int)sched.size();
@@ -274,6 +282,10 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
   out->max_seq_len = max_s;
   out->block_table_stride = stride;
   out->num_decode_reqs = decodes;
+  out->num_context_reqs = ctx_reqs;
+  out->num_context_tokens = ctx_toks;
+  out->num_generation_reqs = gen_reqs;
+  out->num_generation_tokens = gen_toks;
   for (auto& e : sched) {
     e.first->num_computed += e.second;
     if (c.enable_prefix_caching) s->register_full_blocks(e.first);

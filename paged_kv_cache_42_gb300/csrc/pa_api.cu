@@ -7,6 +7,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <mutex>
 
@@ -59,6 +61,13 @@ pa_status device_state(DeviceState** out) {
   *out = &d;
   return PA_OK;
 }
+
+// An NVTX range around a call's launches (header-only NVTX: nothing happens
+// unless a profiler is attached), named after the entry point.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 struct TimerScope {
   int id;
@@ -115,6 +124,7 @@ pa_status write_kv_impl(const void* k, const void* v, const int64_t* slot_mappin
   if (kv_fp8 && !(k_scale > 0.f && k_scale < INFINITY && v_scale > 0.f && v_scale < INFINITY))
     return PA_ERR_INVALID_ARG;
   if (block_size != kBlockSize || head_dim % 8 != 0) return PA_ERR_UNSUPPORTED;
+  const NvtxRange range(kv_fp8 ? "pa_write_kv_fp8" : "pa_write_kv");
   if (num_tokens == 0) return PA_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
@@ -229,6 +239,8 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
 
   DeviceState* d = nullptr;
   if (pa_status st = device_state(&d)) return st;
+  const NvtxRange range(prefix_len > 0 ? "pa_attention_cascade"
+                                       : (kv_fp8 ? "pa_attention_fp8" : "pa_attention"));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
 

@@ -34,7 +34,9 @@ class SchedOutput(ctypes.Structure):
                 ("slot_mapping", _i64p), ("positions", _i32p), ("input_tokens", _i32p),
                 ("preempted_ids", _i64p), ("num_reqs", _c_i), ("num_tokens", _c_i),
                 ("num_preempted", _c_i), ("max_query_len", _c_i), ("max_seq_len", _c_i),
-                ("block_table_stride", _c_i), ("num_decode_reqs", _c_i)]
+                ("block_table_stride", _c_i), ("num_decode_reqs", _c_i),
+                ("num_context_reqs", _c_i), ("num_context_tokens", _c_i),
+                ("num_generation_reqs", _c_i), ("num_generation_tokens", _c_i)]
 
 
 _READY = False
@@ -295,4 +297,14 @@ class Scheduler:
             input_tokens=a["input_tokens"][:T].copy(),
             preempted_ids=a["preempted_ids"][:o.num_preempted].copy(),
             num_tokens=T, max_query_len=o.max_query_len, max_seq_len=o.max_seq_len,
-            num_decode_reqs=o.num_decode_reqs)
+            num_decode_reqs=o.num_decode_reqs, num_context_reqs=o.num_context_reqs,
+            num_context_tokens=o.num_context_tokens, num_generation_reqs=o.num_generation_reqs,
+            num_generation_tokens=o.num_generation_tokens)
+
+
+def step_signature(out: dict) -> str:
+    """Profile name of a scheduled step, execute_context_A(a)_generation_B(b)
+    ("vLLM v1 Deep Dive", Part 3, Step 4c): A requests with a tokens in their
+    prompt (prefill), B requests with b tokens past it (decode)."""
+    return (f"execute_context_{out['num_context_reqs']}({out['num_context_tokens']})"
+            f"_generation_{out['num_generation_reqs']}({out['num_generation_tokens']})")

@@ -272,6 +272,32 @@ def test_lookup_stops_at_first_miss(side):
     pool.release(taken)
 
 
+def _signature(out) -> str:
+    return (f"execute_context_{out['num_context_reqs']}({out['num_context_tokens']})"
+            f"_generation_{out['num_generation_reqs']}({out['num_generation_tokens']})")
+
+
+@pytest.mark.parametrize("ex", range(len(GOLD["step_signature"]["examples"])))
+def test_step_signature_examples(side, ex):
+    """The pages' printed step annotations, reproduced by scheduling the
+    batches they describe: decoding requests first, then whole prompts."""
+    g = GOLD["step_signature"]["examples"][ex]
+    prompts, n_gen = g["context_prompts"], g["decodes"]
+    pool = side.pool(list(range(2000)), 16)
+    s = side.scheduler(pool, token_budget=sum(prompts) + n_gen + 64, max_model_len=2048,
+                       prefix_caching=False)
+    for i in range(n_gen):
+        s.add_request(i, [i + 1] * 3)
+    drive(s, 1)  # their prompts are computed; each now decodes
+    for j, n in enumerate(prompts):
+        s.add_request(1000 + j, [7 + j] * n)
+    out = s.step()
+    assert _signature(out) == g["signature"]
+    if side.name == "library":
+        from paged_kv_cache_42_gb300 import host as h
+        assert h.step_signature(out) == g["signature"]
+
+
 # --------------------------------------------------------------- SHA-256 --
 
 def test_sha256_fips_example(host):
@@ -425,7 +451,9 @@ def random_run(seed: int, lib_host=None, steps: int = 120):
                       "preempted_ids"):
                 assert np.array_equal(np.asarray(got[k]).reshape(-1),
                                       np.asarray(out[k], dtype=np.int64).reshape(-1)), (seed, step, k)
-            for k in ("num_tokens", "max_query_len", "max_seq_len", "num_decode_reqs"):
+            for k in ("num_tokens", "max_query_len", "max_seq_len", "num_decode_reqs",
+                      "num_context_reqs", "num_context_tokens", "num_generation_reqs",
+                      "num_generation_tokens"):
                 assert got[k] == out[k], (seed, step, k)
             assert l_pool.free_queue() == list(o_pool.free), (seed, step)
         for rid in list(out["req_ids"]):
