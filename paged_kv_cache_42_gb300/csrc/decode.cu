@@ -46,6 +46,18 @@ constexpr unsigned kFull = 0xffffffffu;
 // =============================================================================
 // Split-KV decode kernel
 // =============================================================================
+// Largest head group whose P.V pass gives each lane 8 output dims (else 4).
+// Eight dims halve the per-row overhead (address, p broadcast) of the pass at
+// the price of twice the accumulator registers (measured on the Llama-8B
+// decode batch: 98 us against 106 us). PA_DEC_VD8_F8 extends it to an E4M3
+// cache, whose calls otherwise run three CTAs per SM.
+#ifndef PA_DEC_VD8_MAXG
+#define PA_DEC_VD8_MAXG 4
+#endif
+#ifndef PA_DEC_VD8_F8
+#define PA_DEC_VD8_F8 0
+#endif
+
 template <int D, int G, bool F8>
 struct Cfg {
   static constexpr int EB = F8 ? 1 : 2;          // bytes per cached K/V element
@@ -54,7 +66,8 @@ struct Cfg {
   static constexpr int TPP = 32 / TPT;           // tokens per q.k pass
   static constexpr int NPASS = 16 / TPP;
   static constexpr int LOG_G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  static constexpr int LPR = D / 4;   // lanes per V row (4 dims each)
+  static constexpr int VD = (G <= PA_DEC_VD8_MAXG && (!F8 || PA_DEC_VD8_F8)) ? 8 : 4;  // out dims/lane
+  static constexpr int LPR = D / VD;   // lanes per V row
   static constexpr int RPS = 32 / LPR;  // V rows per step
   static constexpr int KV_BYTES = kBlockSize * D * EB;
   static constexpr int Q_BYTES = G * D * 2;
@@ -62,6 +75,7 @@ struct Cfg {
   static constexpr int P_BYTES = kBlockSize * G * 4 + 64;  // p[16][G], alpha[G]
   static_assert(TPT >= G, "a token's lane group must hold one value per head");
   static_assert(DPT == 8 || DPT == 16, "one or two 16-byte chunks per lane");
+  static_assert(RPS >= 1 && kBlockSize % RPS == 0, "whole V rows per step");
 };
 
 template <int D, int G, int NSTAGE, bool F8>
@@ -312,16 +326,16 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   // that avoids bank conflicts; E4M3 rows: one chunk, natural order
   const int swz = (!F8 && C::DPT == 16) ? ((lane >> 2) & 1) : 0;
   const int hsel = head_of_lane<G>(lane);
-  const int rl = lane % C::LPR;                                  // V dims 4*rl .. 4*rl+3
+  const int rl = lane % C::LPR;                                  // V dims VD*rl .. VD*rl+VD-1
   const int rrow = lane / C::LPR;                                // V row within a step
 
   float2 qv[G][C::DPT / 2];
-  float2 acc[G][2];
+  float2 acc[G][C::VD / 2];
   float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    acc[h][0] = make_float2(0.f, 0.f);
-    acc[h][1] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < C::VD / 2; ++i) acc[h][i] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < C::DPT / 2; ++i) qv[h][i] = make_float2(0.f, 0.f);
   }
@@ -391,8 +405,8 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 #pragma unroll
         for (int i = 0; i < C::DPT / 2; ++i)
           qv[h][i] = fmul2(qv[h][i], make_float2(p.scale_log2, p.scale_log2));
-        acc[h][0] = make_float2(0.f, 0.f);
-        acc[h][1] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < C::VD / 2; ++i) acc[h][i] = make_float2(0.f, 0.f);
       }
       m_run = -INFINITY;
       l_run = 0.f;
@@ -482,28 +496,43 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float al = alpha_s[h];
-          acc[h][0] = fmul2(acc[h][0], make_float2(al, al));
-          acc[h][1] = fmul2(acc[h][1], make_float2(al, al));
+#pragma unroll
+          for (int i = 0; i < C::VD / 2; ++i) acc[h][i] = fmul2(acc[h][i], make_float2(al, al));
         }
       }
       // Keys past the sequence end have p = 0; their V rows (which may hold
       // anything, NaN included) are replaced by the last valid row so the
       // loop needs no per-token branch: 0 * finite adds nothing.
-      const unsigned char* const vbase = st_ptr + C::KV_BYTES + rl * 4 * C::EB;
+      const unsigned char* const vbase = st_ptr + C::KV_BYTES + rl * C::VD * C::EB;
       const int tmax = nvalid - 1;
 #pragma unroll
       for (int stp = 0; stp < kBlockSize / C::RPS; ++stp) {
         const int t = stp * C::RPS + rrow;
         {
-          float2 v01, v23;
+          float2 vf[C::VD / 2];
+          const unsigned char* const vrow = vbase + min(t, tmax) * D * C::EB;
           if constexpr (F8) {  // v_scale is applied to the output
-            const uint32_t vv = *reinterpret_cast<const uint32_t*>(vbase + min(t, tmax) * D);
-            v01 = e4m3x2_to_float2((uint16_t)(vv & 0xffffu));
-            v23 = e4m3x2_to_float2((uint16_t)(vv >> 16));
+            if constexpr (C::VD == 8) {
+              const uint2 vv = *reinterpret_cast<const uint2*>(vrow);
+              vf[0] = e4m3x2_to_float2((uint16_t)(vv.x & 0xffffu));
+              vf[1] = e4m3x2_to_float2((uint16_t)(vv.x >> 16));
+              vf[2] = e4m3x2_to_float2((uint16_t)(vv.y & 0xffffu));
+              vf[3] = e4m3x2_to_float2((uint16_t)(vv.y >> 16));
+            } else {
+              const uint32_t vv = *reinterpret_cast<const uint32_t*>(vrow);
+              vf[0] = e4m3x2_to_float2((uint16_t)(vv & 0xffffu));
+              vf[1] = e4m3x2_to_float2((uint16_t)(vv >> 16));
+            }
+          } else if constexpr (C::VD == 8) {
+            const uint4 vv = *reinterpret_cast<const uint4*>(vrow);
+            vf[0] = bf16x2_to_float2(vv.x);
+            vf[1] = bf16x2_to_float2(vv.y);
+            vf[2] = bf16x2_to_float2(vv.z);
+            vf[3] = bf16x2_to_float2(vv.w);
           } else {
-            const uint2 vv = *reinterpret_cast<const uint2*>(vbase + min(t, tmax) * D * 2);
-            v01 = bf16x2_to_float2(vv.x);
-            v23 = bf16x2_to_float2(vv.y);
+            const uint2 vv = *reinterpret_cast<const uint2*>(vrow);
+            vf[0] = bf16x2_to_float2(vv.x);
+            vf[1] = bf16x2_to_float2(vv.y);
           }
           float2 ph[G];
           if constexpr (G >= 4) {
@@ -524,8 +553,8 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
           }
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            acc[h][0] = ffma2(ph[h], v01, acc[h][0]);
-            acc[h][1] = ffma2(ph[h], v23, acc[h][1]);
+#pragma unroll
+            for (int i = 0; i < C::VD / 2; ++i) acc[h][i] = ffma2(ph[h], vf[i], acc[h][i]);
           }
         }
       }
@@ -571,21 +600,40 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
         mh[h] = __shfl_sync(kFull, m_run, src);
         lh[h] = __shfl_sync(kFull, lsum, src);
       }
-      if constexpr (C::RPS == 2) {
+      // the RPS row groups of the P.V pass each hold part of every output dim
+#pragma unroll
+      for (int o = C::LPR; o < 32; o <<= 1) {
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          acc[h][0].x += __shfl_xor_sync(kFull, acc[h][0].x, 16);
-          acc[h][0].y += __shfl_xor_sync(kFull, acc[h][0].y, 16);
-          acc[h][1].x += __shfl_xor_sync(kFull, acc[h][1].x, 16);
-          acc[h][1].y += __shfl_xor_sync(kFull, acc[h][1].y, 16);
+#pragma unroll
+          for (int i = 0; i < C::VD / 2; ++i) {
+            acc[h][i].x += __shfl_xor_sync(kFull, acc[h][i].x, o);
+            acc[h][i].y += __shfl_xor_sync(kFull, acc[h][i].y, o);
+          }
         }
       }
       const int ustart = y - blk;  // first position of this (token, kv head)
       const int wf = worker_of(ustart), wl = worker_of(ustart + nb - 1);
-      uint16_t* orow = p.out + ((size_t)tok * Hq + (size_t)kv * G) * D + rl * 4;
+      uint16_t* orow = p.out + ((size_t)tok * Hq + (size_t)kv * G) * D + rl * C::VD;
+      // the lane's VD output dims of head h, scaled by f, as bf16
+      auto store_out = [&](int h, const float* o, float f) {
+        if constexpr (C::VD == 8) {
+          uint4 pk;
+          pk.x = float2_to_bf16x2(o[0] * f, o[1] * f);
+          pk.y = float2_to_bf16x2(o[2] * f, o[3] * f);
+          pk.z = float2_to_bf16x2(o[4] * f, o[5] * f);
+          pk.w = float2_to_bf16x2(o[6] * f, o[7] * f);
+          *reinterpret_cast<uint4*>(orow + h * D) = pk;
+        } else {
+          uint2 pk;
+          pk.x = float2_to_bf16x2(o[0] * f, o[1] * f);
+          pk.y = float2_to_bf16x2(o[2] * f, o[3] * f);
+          *reinterpret_cast<uint2*>(orow + h * D) = pk;
+        }
+      };
       // Cascade: the prefix partials of this (token, kv head), one per key
       // chunk, folded into (M, Ls, O) by log-sum-exp renormalisation.
-      auto fold_prefix = [&](float (&M)[G], float (&Ls)[G], float4 (&O)[G]) {
+      auto fold_prefix = [&](float (&M)[G], float (&Ls)[G], float (&O)[G][C::VD]) {
 #pragma unroll 1
         for (int c = 0; c < p.prefix_chunks; ++c) {
           const float* sl =
@@ -596,45 +644,48 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
             const float ms = __ldcg(sl + h);
             const float mn = fmaxf(M[h], ms);
             const float a = exp2f(M[h] - mn), b = exp2f(ms - mn);
-            const float4 o = __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D + rl * 4));
             Ls[h] = Ls[h] * a + __ldcg(sl + G + h) * b;
-            O[h].x = O[h].x * a + o.x * b;
-            O[h].y = O[h].y * a + o.y * b;
-            O[h].z = O[h].z * a + o.z * b;
-            O[h].w = O[h].w * a + o.w * b;
+#pragma unroll
+            for (int i = 0; i < C::VD / 4; ++i) {
+              const float4 o =
+                  __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D + rl * C::VD) + i);
+              O[h][4 * i] = O[h][4 * i] * a + o.x * b;
+              O[h][4 * i + 1] = O[h][4 * i + 1] * a + o.y * b;
+              O[h][4 * i + 2] = O[h][4 * i + 2] * a + o.z * b;
+              O[h][4 * i + 3] = O[h][4 * i + 3] * a + o.w * b;
+            }
             M[h] = mn;
           }
         }
       };
       if (wf == wl) {
         if (p.prefix_partials) {
-          float M[G], Ls[G];
-          float4 O[G];
+          float M[G], Ls[G], O[G][C::VD];
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             M[h] = mh[h];
             Ls[h] = lh[h];
-            O[h] = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+#pragma unroll
+            for (int i = 0; i < C::VD / 2; ++i) {
+              O[h][2 * i] = acc[h][i].x;
+              O[h][2 * i + 1] = acc[h][i].y;
+            }
           }
           fold_prefix(M, Ls, O);
           if (rrow == 0) {
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const float inv = p.v_scale / Ls[h];
-              uint2 pk;
-              pk.x = float2_to_bf16x2(O[h].x * inv, O[h].y * inv);
-              pk.y = float2_to_bf16x2(O[h].z * inv, O[h].w * inv);
-              *reinterpret_cast<uint2*>(orow + h * D) = pk;
-            }
+            for (int h = 0; h < G; ++h) store_out(h, O[h], p.v_scale / Ls[h]);
           }
         } else if (rrow == 0) {
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float inv = p.v_scale / lh[h];
-            uint2 pk;
-            pk.x = float2_to_bf16x2(acc[h][0].x * inv, acc[h][0].y * inv);
-            pk.y = float2_to_bf16x2(acc[h][1].x * inv, acc[h][1].y * inv);
-            *reinterpret_cast<uint2*>(orow + h * D) = pk;
+            float o[C::VD];
+#pragma unroll
+            for (int i = 0; i < C::VD / 2; ++i) {
+              o[2 * i] = acc[h][i].x;
+              o[2 * i + 1] = acc[h][i].y;
+            }
+            store_out(h, o, p.v_scale / lh[h]);
           }
         }
       } else {
@@ -651,9 +702,13 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
         }
         if (rrow == 0) {
 #pragma unroll
-          for (int h = 0; h < G; ++h)
-            __stcg(reinterpret_cast<float4*>(slot + 16 + h * D + rl * 4),
-                   make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y));
+          for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int i = 0; i < C::VD / 4; ++i)
+              __stcg(reinterpret_cast<float4*>(slot + 16 + h * D + rl * C::VD) + i,
+                     make_float4(acc[h][2 * i].x, acc[h][2 * i].y, acc[h][2 * i + 1].x,
+                                 acc[h][2 * i + 1].y));
+          }
         }
         __threadfence();
         __syncwarp();
@@ -668,13 +723,13 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
         prev = __shfl_sync(kFull, prev, 0);
         if (prev == wl - wf) {  // every other segment has landed: merge them all
           __threadfence();
-          float M[G], Ls[G];
-          float4 O[G];
+          float M[G], Ls[G], O[G][C::VD];
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             M[h] = -INFINITY;
             Ls[h] = 0.f;
-            O[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < C::VD; ++i) O[h][i] = 0.f;
           }
 #pragma unroll 1
           for (int s = wf; s <= wl; ++s) {
@@ -689,23 +744,21 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
             for (int h = 0; h < G; ++h) {
               const float f = exp2f(__ldcg(sl + h) - M[h]);
               Ls[h] += __ldcg(sl + G + h) * f;
-              const float4 o = __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D + rl * 4));
-              O[h].x += o.x * f;
-              O[h].y += o.y * f;
-              O[h].z += o.z * f;
-              O[h].w += o.w * f;
+#pragma unroll
+              for (int i = 0; i < C::VD / 4; ++i) {
+                const float4 o =
+                    __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D + rl * C::VD) + i);
+                O[h][4 * i] += o.x * f;
+                O[h][4 * i + 1] += o.y * f;
+                O[h][4 * i + 2] += o.z * f;
+                O[h][4 * i + 3] += o.w * f;
+              }
             }
           }
           if (p.prefix_partials) fold_prefix(M, Ls, O);
           if (rrow == 0) {
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const float inv = p.v_scale / Ls[h];
-              uint2 pk;
-              pk.x = float2_to_bf16x2(O[h].x * inv, O[h].y * inv);
-              pk.y = float2_to_bf16x2(O[h].z * inv, O[h].w * inv);
-              *reinterpret_cast<uint2*>(orow + h * D) = pk;
-            }
+            for (int h = 0; h < G; ++h) store_out(h, O[h], p.v_scale / Ls[h]);
           }
         }
       }
