@@ -110,7 +110,7 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
 
 /*
  * Bytes of device workspace pa_attention needs for a batch of this size
- * (planner output, split-KV partial results and merge counters). The value
+ * (planner output and split-KV partial results). The value
  * depends only on the arguments, not on the device. Returns 0 on bad
  * arguments.
  */
@@ -287,7 +287,8 @@ pa_status pa_get_device_error(int* code, long long* detail, int clear);
  * Instrumentation: record `start_event` / `stop_event` (cudaEvent_t handles
  * created by the caller) around every later launch of the given kernel on its
  * stream; pass NULL events to stop. Kernel ids: 0 write_kv, 1 planner,
- * 2 decode (split-KV), 3 prefill chunk, 4 cascade prefix pass. Process-wide setting, not thread-safe.
+ * 2 decode (split-KV), 3 prefill chunk, 4 cascade prefix pass, 5 split-KV
+ * merge pass. Process-wide setting, not thread-safe.
  */
 pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event);
 
@@ -295,10 +296,10 @@ pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event
  * Process-wide options.
  *   PA_OPT_DECODE_SELF_PLAN (default 1): a batch whose spans are all at most
  *     one token (pure decode), with at most 512 requests and no cascade, is
- *     planned inside the split-KV kernel. That kernel then starts streaming
- *     K/V without waiting for the planner or for the preceding KV write; it
- *     waits for them (griddepcontrol.wait) only before reading a request's
- *     last block, which holds the newest token, and before its first merge.
+ *     planned inside the split-KV kernel, and the planner is not launched.
+ *     That kernel then starts streaming K/V without waiting for the preceding
+ *     KV write; it waits for it (griddepcontrol.wait) only before reading a
+ *     request's last block, which holds the newest token.
  *     The results are bit-identical with the option off (the planner path),
  *     which the tests compare. value 0 turns it off.
  * PA_ERR_INVALID_ARG for an unknown option. Not thread-safe.

@@ -28,7 +28,7 @@ STATUS = {0: "PA_OK", -1: "PA_ERR_INVALID_ARG", -2: "PA_ERR_UNSUPPORTED",
 DEVICE_ERRORS = {0: "none", 1: "slot outside the pool", 2: "block id outside the pool",
                  3: "inconsistent lengths", 4: "query_start_loc out of range",
                  5: "bounded wait timed out", 6: "table does not start with the common prefix"}
-KERNEL_IDS = {"write_kv": 0, "plan": 1, "decode": 2, "prefill": 3, "prefix": 4}
+KERNEL_IDS = {"write_kv": 0, "plan": 1, "decode": 2, "prefill": 3, "prefix": 4, "merge": 5}
 
 
 class PagedAttentionError(RuntimeError):

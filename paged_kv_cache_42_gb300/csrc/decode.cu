@@ -17,11 +17,11 @@
 // independent worker that takes one contiguous, equally sized slice of that
 // sequence, so the load balance is exact whatever the length mix. A warp
 // whose slice holds a whole (token, kv head) writes the output directly;
-// otherwise it writes an unnormalised partial (o, m, l) and the last warp to
-// finish that (token, kv head) merges the partials by log-sum-exp
-// renormalisation ("vLLM: An Exhaustive Technical Study for Kernel
-// Engineers", 2.3, cascade attention's log-sum-exp merge) - no second kernel,
-// no spin-wait, a fixed merge order (deterministic results).
+// otherwise it writes an unnormalised partial (o, m, l) and moves on, and the
+// merge pass (merge.cu), chained after this grid, combines the partials by
+// log-sum-exp renormalisation ("vLLM: An Exhaustive Technical Study for
+// Kernel Engineers", 2.3, cascade attention's log-sum-exp merge) in a fixed
+// order (deterministic results). No warp waits on another.
 //
 // Data movement. Each (block, kv head) of K and of V is one contiguous
 // 16 x D bf16 tile in the cache, fetched whole with a 1-D bulk async copy
@@ -49,13 +49,10 @@ constexpr unsigned kFull = 0xffffffffu;
 // Largest head group whose P.V pass gives each lane 8 output dims (else 4).
 // Eight dims halve the per-row overhead (address, p broadcast) of the pass at
 // the price of twice the accumulator registers (measured on the Llama-8B
-// decode batch: 98 us against 106 us). PA_DEC_VD8_F8 extends it to an E4M3
-// cache, whose calls otherwise run three CTAs per SM.
+// decode batch: 98 us against 106 us with a bf16 cache, 106 us against
+// 108 us with an E4M3 one, although its two CTAs per SM replace three).
 #ifndef PA_DEC_VD8_MAXG
 #define PA_DEC_VD8_MAXG 4
-#endif
-#ifndef PA_DEC_VD8_F8
-#define PA_DEC_VD8_F8 0
 #endif
 
 template <int D, int G, bool F8>
@@ -66,7 +63,7 @@ struct Cfg {
   static constexpr int TPP = 32 / TPT;           // tokens per q.k pass
   static constexpr int NPASS = 16 / TPP;
   static constexpr int LOG_G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  static constexpr int VD = (G <= PA_DEC_VD8_MAXG && (!F8 || PA_DEC_VD8_F8)) ? 8 : 4;  // out dims/lane
+  static constexpr int VD = G <= PA_DEC_VD8_MAXG ? 8 : 4;  // output dims per lane
   static constexpr int LPR = D / VD;   // lanes per V row
   static constexpr int RPS = 32 / LPR;  // V rows per step
   static constexpr int KV_BYTES = kBlockSize * D * EB;
@@ -140,6 +137,9 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   using C = Cfg<D, G, F8>;
   using WS = WarpSmem<D, G, NSTAGE, F8>;
   extern __shared__ __align__(128) unsigned char smem[];
+  // The merge pass may be placed as soon as CTAs of this persistent grid
+  // retire (it waits for the whole grid before reading).
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned char* const wsm = smem + warp * WS::BYTES;  // this warp's region
   const uint32_t stage0 = smem_u32(wsm);
@@ -198,6 +198,10 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     }
     if (threadIdx.x == 0) su[R] = UnitInfo{T, -1, 0, carry};
     __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0) {  // the merge pass slices alike
+      p.header_out->num_units = R;
+      p.header_out->num_positions = carry;
+    }
     units = su;
     W = carry;
     K = R;
@@ -211,13 +215,12 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   const int NW = plan_workers(W, gridDim.x * WARPS);
   const int w = blockIdx.x * WARPS + warp;
   if (w >= NW) return;
-  const int S = (int)((long long)w * W / NW);
-  const int E = (int)((long long)(w + 1) * W / NW);
+  const int S = worker_begin(w, W, NW);
+  const int E = worker_begin(w + 1, W, NW);
   if (S >= E) return;
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
   const int kstart = p.key_start_blocks;  // first block on this path (cascade prefix skipped)
 
-  auto worker_of = [&](int x) -> int { return (int)(((long long)(x + 1) * NW - 1) / W); };
 
   // ---- batch metadata helpers ------------------------------------------------
   auto window = [&](int kbase) -> int {
@@ -280,6 +283,19 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 
   Batch cur = finish(S, locate(S, lo, window(lo)));
   Batch nxt = cur;
+  if (w > 0) {  // the merge task of the slice boundary before this worker
+    const int tok0 = __shfl_sync(kFull, cur.tok, 0), kv0 = __shfl_sync(kFull, cur.kv, 0);
+    const int blk0 = __shfl_sync(kFull, cur.blk, 0), nb0 = __shfl_sync(kFull, cur.nb, 0);
+    if (lane == 0) {
+      int4 task = make_int4(-1, 0, 0, 0);
+      if (blk0 != 0) {  // the slice starts inside a (token, kv head)
+        const int first = S - blk0;
+        const int wf = worker_of(first, W, NW);
+        if (w == wf + 1) task = make_int4(tok0, kv0, wf, worker_of(first + nb0 - 1, W, NW));
+      }
+      p.merge_tasks[w] = task;
+    }
+  }
   int y0 = S;
   int nwin = 0, nkbase = 0;
   Loc nkl{0, 0, 0, 0, 0};
@@ -613,7 +629,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
         }
       }
       const int ustart = y - blk;  // first position of this (token, kv head)
-      const int wf = worker_of(ustart), wl = worker_of(ustart + nb - 1);
+      const int wf = worker_of(ustart, W, NW), wl = worker_of(ustart + nb - 1, W, NW);
       uint16_t* orow = p.out + ((size_t)tok * Hq + (size_t)kv * G) * D + rl * C::VD;
       // the lane's VD output dims of head h, scaled by f, as bf16
       auto store_out = [&](int h, const float* o, float f) {
@@ -689,8 +705,8 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
           }
         }
       } else {
-        // merge slot and counter of this (token, kv head): tokens increase with
-        // the position order, so slot u + worker is unique per segment
+        // a partial (m, l, o) for the merge pass, in slot u + w: tokens
+        // increase with the position order, so the slot is unique per segment
         const int u = tok * Hkv + kv;
         float* slot = p.partials + (size_t)(u + w) * p.slot_floats;
         if (lane == 0) {
@@ -708,57 +724,6 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
               __stcg(reinterpret_cast<float4*>(slot + 16 + h * D + rl * C::VD) + i,
                      make_float4(acc[h][2 * i].x, acc[h][2 * i].y, acc[h][2 * i + 1].x,
                                  acc[h][2 * i + 1].y));
-          }
-        }
-        __threadfence();
-        __syncwarp();
-        int prev = 0;
-        if (lane == 0) {
-          if (!waited) {  // the counters are zeroed by the planner
-            griddep_wait();
-            waited = true;
-          }
-          prev = atomicAdd(p.counters + u, 1);
-        }
-        prev = __shfl_sync(kFull, prev, 0);
-        if (prev == wl - wf) {  // every other segment has landed: merge them all
-          __threadfence();
-          float M[G], Ls[G], O[G][C::VD];
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            M[h] = -INFINITY;
-            Ls[h] = 0.f;
-#pragma unroll
-            for (int i = 0; i < C::VD; ++i) O[h][i] = 0.f;
-          }
-#pragma unroll 1
-          for (int s = wf; s <= wl; ++s) {
-            const float* sl = p.partials + (size_t)(u + s) * p.slot_floats;
-#pragma unroll
-            for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(sl + h));
-          }
-#pragma unroll 1
-          for (int s = wf; s <= wl; ++s) {
-            const float* sl = p.partials + (size_t)(u + s) * p.slot_floats;
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              const float f = exp2f(__ldcg(sl + h) - M[h]);
-              Ls[h] += __ldcg(sl + G + h) * f;
-#pragma unroll
-              for (int i = 0; i < C::VD / 4; ++i) {
-                const float4 o =
-                    __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D + rl * C::VD) + i);
-                O[h][4 * i] += o.x * f;
-                O[h][4 * i + 1] += o.y * f;
-                O[h][4 * i + 2] += o.z * f;
-                O[h][4 * i + 3] += o.w * f;
-              }
-            }
-          }
-          if (p.prefix_partials) fold_prefix(M, Ls, O);
-          if (rrow == 0) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) store_out(h, O[h], p.v_scale / Ls[h]);
           }
         }
       }
@@ -804,12 +769,14 @@ cudaError_t decode_grid(int num_sms, int occ_cap, bool self_plan, int* grid_out)
 }
 
 template <int D, int G, int WARPS, int NSTAGE, bool F8>
-cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s) {
+cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s,
+                            int* workers_out) {
   auto kern = pa_decode_kernel<D, G, WARPS, NSTAGE, F8>;
   const int smem = decode_smem<D, G, WARPS, NSTAGE, F8>(p.self_plan != 0);
   int grid = 0;
   cudaError_t e = decode_grid<D, G, WARPS, NSTAGE, F8>(num_sms, occ_cap, p.self_plan != 0, &grid);
   if (e != cudaSuccess) return e;
+  *workers_out = grid * WARPS;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(WARPS * 32);
@@ -820,7 +787,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   // Programmatic launch: the grid starts when the preceding grid triggers
-  // (the planner at its top for a self-planned batch, otherwise at its end).
+  // (the KV write at its top for a self-planned batch, which has no planner;
+  // otherwise the planner or the tensor-core grid, at their end).
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
@@ -855,9 +823,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, int num_sms, int occ_cap, cud
 #endif
 
 // Warps per CTA and ring stages per warp of each instantiation. An E4M3 tile
-// is half the bytes of a bf16 one: three-stage FP8 rings leave room for three
-// CTAs per SM (the FP8 calls run three; measured: the stage count itself
-// hardly matters, the extra warps do).
+// is half the bytes of a bf16 one: three-stage FP8 rings still leave room for
+// a third CTA per SM where registers allow it (groups of up to two heads).
 template <int D, int G, bool F8>
 struct Tuning {
   static constexpr int WARPS =
@@ -868,9 +835,10 @@ struct Tuning {
 };
 
 template <int D, int G, bool F8>
-cudaError_t launch_one(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s) {
+cudaError_t launch_one(const DecodeParams& p, int num_sms, int occ_cap, cudaStream_t s,
+                       int* workers_out) {
   using T = Tuning<D, G, F8>;
-  return launch_decode_t<D, G, T::WARPS, T::STAGES, F8>(p, num_sms, occ_cap, s);
+  return launch_decode_t<D, G, T::WARPS, T::STAGES, F8>(p, num_sms, occ_cap, s, workers_out);
 }
 
 template <int D, int G, bool F8>
@@ -904,8 +872,8 @@ int workers_one(int num_sms, int occ_cap) {
   } while (0)
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool f8, int num_sms,
-                          int occ_cap, cudaStream_t s) {
-  PA_DECODE_DISPATCH(launch_one, cudaErrorInvalidValue, p, num_sms, occ_cap, s);
+                          int occ_cap, cudaStream_t s, int* workers_out) {
+  PA_DECODE_DISPATCH(launch_one, cudaErrorInvalidValue, p, num_sms, occ_cap, s, workers_out);
 }
 
 int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap) {

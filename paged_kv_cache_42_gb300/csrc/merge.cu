@@ -1,0 +1,158 @@
+// Merge pass of the split-KV decode.
+//
+// The split-KV kernel gives each warp an equal slice of the flattened
+// (token, kv head, 16-key block) positions. A (token, kv head) whose blocks
+// fall into more than one slice leaves one unnormalised partial (m, l, o)
+// per slice, in slots u + wf .. u + wl (u = token * Hkv + kv head, wf .. wl
+// the workers whose slices hold its first and last block). This pass runs
+// after the split-KV grid (chained by programmatic launch, it waits on that
+// grid before reading) and combines them by log-sum-exp renormalisation
+// ("vLLM: An Exhaustive Technical Study for Kernel Engineers", 2.3, the merge
+// of partial attention states) in a fixed order of operations, so the result
+// does not depend on which warp finished first. In a cascade call the prefix
+// partials of the same (token, kv head) are merged in with the suffix slots.
+//
+// One CTA per slice boundary, reading the task the split-KV worker after the
+// boundary left for it. Its warps split the partials between them, each
+// merging its share online (the loads of the next partial are independent of
+// the arithmetic), and combine their results through shared memory; so a
+// merge takes about one round trip to L2 whatever the number of partials.
+#include "pa_internal.h"
+#include "ptx.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMergeWarps = 4;
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeParams p) {
+  constexpr int V = D / 32;  // output dims per lane
+  static_assert(V == 2 || V == 4, "head dim 64 or 128");
+  __shared__ float s_m[kMergeWarps][G], s_l[kMergeWarps][G];
+  __shared__ __align__(16) float s_o[kMergeWarps][G][D];
+  griddep_wait();  // the split-KV grid's partials and tasks
+  const int w = blockIdx.x + 1;
+  const int W = __ldcg(&p.header->num_positions);
+  const int4 task = __ldcg(p.tasks + w);
+  // tasks past this call's worker count are stale
+  if (W <= 0 || w >= plan_workers(W, p.num_workers) || task.x < 0) return;
+  const int tok = task.x, kv = task.y, wf = task.z, wl = task.w;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // The partials: the suffix slots wf .. wl, then (cascade) the prefix chunks.
+  const int u = tok * p.num_kv_heads + kv;
+  const int ns = wl - wf + 1, n = ns + p.prefix_chunks;
+  auto slot = [&](int i) -> const float* {
+    return i < ns ? p.partials + (size_t)(u + wf + i) * p.slot_floats
+                  : p.prefix_partials +
+                        (((size_t)(i - ns) * p.num_tokens + tok) * p.num_kv_heads + kv) *
+                            p.slot_floats;
+  };
+
+  // this warp's share: partials warp, warp + kMergeWarps, ...
+  float M[G], L[G], O[G][V];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    M[h] = -INFINITY;
+    L[h] = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) O[h][i] = 0.f;
+  }
+#pragma unroll 2
+  for (int i = warp; i < n; i += kMergeWarps) {
+    const float* sl = slot(i);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float m = __ldcg(sl + h), l = __ldcg(sl + G + h);
+      float o[V];
+      if constexpr (V == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D) + lane);
+        o[0] = v.x;
+        o[1] = v.y;
+        o[2] = v.z;
+        o[3] = v.w;
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(sl + 16 + h * D) + lane);
+        o[0] = v.x;
+        o[1] = v.y;
+      }
+      const float mn = fmaxf(M[h], m);
+      const float a = exp2f(M[h] - mn), b = exp2f(m - mn);  // M = -inf at first: a = 0
+      L[h] = L[h] * a + l * b;
+#pragma unroll
+      for (int i2 = 0; i2 < V; ++i2) O[h][i2] = O[h][i2] * a + o[i2] * b;
+      M[h] = mn;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    if (lane == 0) {
+      s_m[warp][h] = M[h];
+      s_l[warp][h] = L[h];
+    }
+#pragma unroll
+    for (int i = 0; i < V; ++i) s_o[warp][h][lane * V + i] = O[h][i];
+  }
+  __syncthreads();
+
+  // combine the warps' shares (a warp without partials has m = -inf)
+  for (int e = threadIdx.x; e < G * D; e += kMergeWarps * 32) {
+    const int h = e / D, d = e - h * D;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMergeWarps; ++k) mx = fmaxf(mx, s_m[k][h]);
+    float l = 0.f, o = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMergeWarps; ++k) {
+      const float f = s_m[k][h] == -INFINITY ? 0.f : exp2f(s_m[k][h] - mx);
+      l += s_l[k][h] * f;
+      o += s_o[k][h][d] * f;
+    }
+    p.out[((size_t)tok * p.num_q_heads + (size_t)kv * G + h) * D + d] =
+        (uint16_t)(float2_to_bf16x2(o * (p.v_scale / l), 0.f) & 0xffffu);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
+  const int boundaries = p.num_workers - 1;
+  if (boundaries <= 0) return cudaSuccess;  // one worker: nothing is ever split
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)boundaries);  // one CTA per slice boundary
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  // Programmatic launch: the CTAs are placed as the split-KV grid's CTAs
+  // retire and wait (griddepcontrol.wait) for the whole grid before reading.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa_merge_kernel<D, G>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, int head_dim, int group, cudaStream_t s) {
+  if (head_dim == 128) {
+    switch (group) {
+      case 1: return launch_merge_t<128, 1>(p, s);
+      case 2: return launch_merge_t<128, 2>(p, s);
+      case 4: return launch_merge_t<128, 4>(p, s);
+      case 8: return launch_merge_t<128, 8>(p, s);
+    }
+  } else if (head_dim == 64) {
+    switch (group) {
+      case 1: return launch_merge_t<64, 1>(p, s);
+      case 2: return launch_merge_t<64, 2>(p, s);
+      case 4: return launch_merge_t<64, 4>(p, s);
+      case 8: return launch_merge_t<64, 8>(p, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

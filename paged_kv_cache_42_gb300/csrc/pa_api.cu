@@ -35,7 +35,7 @@ std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<long long> g_launches{0};
 std::atomic<int> g_self_plan{1};  // pa_set_option(PA_OPT_DECODE_SELF_PLAN, ...)
-constexpr int kNumTimers = 5;  // write, plan, decode, prefill, cascade prefix
+constexpr int kNumTimers = 6;  // write, plan, decode, prefill, cascade prefix, merge
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
 
@@ -262,11 +262,10 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   pp.block_tables = block_tables;
   pp.prefix_blocks = prefix_len / kBlockSize;
   // a decode-only batch (every span at most one token) plans itself inside
-  // the split-KV kernel, which then overlaps the planner and the KV write
+  // the split-KV kernel: no planner launch, and the kernel overlaps the KV write
   const int self_plan = (g_self_plan.load() && prefix_len == 0 && max_query_len <= 1 &&
                          num_reqs <= kSelfPlanMaxReqs) ? 1 : 0;
-  pp.self_plan = self_plan;
-  pp.early_trigger = (self_plan || prefix_len > 0) ? 1 : 0;
+  pp.early_trigger = prefix_len > 0 ? 1 : 0;
   pp.num_reqs = num_reqs;
   pp.num_tokens = num_tokens;
   pp.num_kv_heads = num_kv_heads;
@@ -282,12 +281,11 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   if (pp.num_workers <= 0) return PA_ERR_CUDA;
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
   pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
-  pp.counters = reinterpret_cast<int*>(ws + lay.counters_off);
   pp.tiles = reinterpret_cast<PrefillTile*>(ws + lay.tiles_off);
   pp.raw = reinterpret_cast<int2*>(ws + lay.raw_off);
   pp.worker_unit = reinterpret_cast<int*>(ws + lay.workers_off);
   pp.err = d->err;
-  {
+  if (!self_plan) {
     TimerScope timer(1, s);
     const cudaError_t e = launch_plan(pp, s);
     g_launches.fetch_add(1);
@@ -341,7 +339,6 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   dp.header = pp.header;
   dp.units = pp.units;
   dp.worker_unit = num_tokens <= kPlanSmemTokens ? pp.worker_unit : nullptr;
-  dp.counters = pp.counters;
   dp.partials = reinterpret_cast<float*>(ws + lay.partials_off);
   dp.slot_floats = lay.slot_floats;
   dp.key_start_blocks = prefix_len / kBlockSize;
@@ -355,12 +352,35 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   dp.max_seq_len = max_seq_len;
   dp.qsl = query_start_loc;
   dp.seq_lens = seq_lens;
+  dp.header_out = pp.header;
+  dp.merge_tasks = reinterpret_cast<int4*>(ws + lay.tasks_off);
   dp.err = d->err;
+  int workers = 0;
   {
     TimerScope timer(2, s);
-    const cudaError_t e =
-        launch_decode(dp, head_dim, num_q_heads / num_kv_heads, kv_fp8 != 0, d->num_sms, occ_cap,
-                      s);
+    const cudaError_t e = launch_decode(dp, head_dim, group, kv_fp8 != 0, d->num_sms, occ_cap, s,
+                                        &workers);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
+
+  MergeParams mp;
+  mp.header = pp.header;
+  mp.tasks = dp.merge_tasks;
+  mp.partials = dp.partials;
+  mp.slot_floats = lay.slot_floats;
+  mp.num_workers = workers;
+  mp.num_q_heads = num_q_heads;
+  mp.num_kv_heads = num_kv_heads;
+  mp.num_tokens = num_tokens;
+  mp.key_start_blocks = dp.key_start_blocks;
+  mp.prefix_partials = prefix_partials;
+  mp.prefix_chunks = chunks;
+  mp.v_scale = dp.v_scale;
+  mp.out = dp.out;
+  if (workers > 1) {
+    TimerScope timer(5, s);
+    const cudaError_t e = launch_merge(mp, head_dim, group, s);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }

@@ -31,6 +31,15 @@ __host__ __device__ inline int plan_workers(int W, int all) {
   int n = W / PA_DEC_MIN_POS;
   return n < 1 ? 1 : (n > all ? all : n);
 }
+// Worker w of NW takes positions [worker_begin(w), worker_begin(w + 1)) of
+// the W flattened positions; worker_of(x) is the worker that takes x. The
+// split-KV kernel and the merge pass must slice alike.
+__host__ __device__ inline int worker_begin(int w, int W, int NW) {
+  return (int)((long long)w * W / NW);
+}
+__host__ __device__ inline int worker_of(int x, int W, int NW) {
+  return (int)(((long long)(x + 1) * NW - 1) / W);
+}
 
 // One entry per token that has keys to attend to, in token order (the
 // planner compacts away tokens with no work). `base` is the first position
@@ -68,7 +77,7 @@ static_assert(sizeof(WsHeader) == 256, "header occupies the first 256 bytes");
 
 // Workspace carve-up, identical on host and device.
 struct WsLayout {
-  size_t header_off, units_off, counters_off, tiles_off, raw_off, workers_off, partials_off, total;
+  size_t header_off, units_off, tiles_off, raw_off, workers_off, tasks_off, partials_off, total;
   int slot_floats;  // floats per partial-result slot
 };
 
@@ -81,14 +90,13 @@ __host__ __device__ inline WsLayout ws_layout(int num_reqs, int num_tokens, int 
   l.slot_floats = 16 + G * head_dim;  // [m x G][l x G] padded to 16 floats, then o[G][D]
   l.header_off = 0;
   l.units_off = pa_align256(sizeof(WsHeader));
-  l.counters_off = l.units_off + pa_align256(sizeof(UnitInfo) * (size_t)(num_tokens + 1));
-  l.tiles_off =
-      l.counters_off + pa_align256(sizeof(int) * (size_t)num_tokens * (size_t)num_kv_heads);
+  l.tiles_off = l.units_off + pa_align256(sizeof(UnitInfo) * (size_t)(num_tokens + 1));
   // a chunk of qlen tokens makes ceil(qlen / (128 / G)) <= qlen / 16 + 1 tiles per kv head
   const size_t max_tiles = (size_t)num_kv_heads * ((size_t)num_tokens / 16 + (size_t)num_reqs + 1);
   l.raw_off = l.tiles_off + pa_align256(sizeof(PrefillTile) * max_tiles);
   l.workers_off = l.raw_off + pa_align256(8 * (size_t)num_tokens);
-  l.partials_off = l.workers_off + pa_align256(sizeof(int) * (size_t)kMaxDecodeWorkers);
+  l.tasks_off = l.workers_off + pa_align256(sizeof(int) * (size_t)kMaxDecodeWorkers);
+  l.partials_off = l.tasks_off + pa_align256(sizeof(int4) * (size_t)kMaxDecodeWorkers);
   const size_t slots = (size_t)num_tokens * num_kv_heads + kMaxDecodeWorkers;
   l.total = l.partials_off + pa_align256(sizeof(float) * (size_t)l.slot_floats * slots);
   return l;
@@ -135,8 +143,6 @@ struct PlanParams {
   const int32_t* seq_lens;
   const int32_t* block_tables;  // read only for the cascade prefix check
   int prefix_blocks;            // cascade: blocks of the common prefix; 0 otherwise
-  int self_plan;                // decode-only batch planned by the split-KV kernel: only
-                                // zero the merge counters
   int early_trigger;            // release the next grid at the top (it needs no plan at first)
   int num_reqs, num_tokens, num_kv_heads, max_blocks_per_req, max_query_len, max_seq_len;
   int group;        // G = Hq / Hkv
@@ -144,7 +150,6 @@ struct PlanParams {
   int num_workers;  // split-KV workers the decode launch provides
   WsHeader* header;
   UnitInfo* units;
-  int* counters;
   PrefillTile* tiles;
   int2* raw;        // per-token scratch when the batch is too large for shared memory
   int* worker_unit; // first unit of each split-KV worker (only when the batch fits)
@@ -187,7 +192,6 @@ struct DecodeParams {
   const WsHeader* header;
   const UnitInfo* units;
   const int* worker_unit;  // null: each worker searches for its first unit
-  int* counters;
   float* partials;
   int slot_floats;
   // cascade: keys start after the common prefix, whose partials are merged in
@@ -195,10 +199,35 @@ struct DecodeParams {
   const float* prefix_partials;  // null without a cascade
   int prefix_chunks, num_tokens;
   // self-planned decode-only batch: the kernel builds its unit table from these
+  // and its first CTA publishes the position count (header_out) for the merge pass
   int self_plan, num_reqs, max_blocks_per_req, max_query_len, max_seq_len;
   const int32_t* qsl;
   const int32_t* seq_lens;
+  WsHeader* header_out;
+  // merge task of the slice boundary before each worker (see MergeParams)
+  int4* merge_tasks;
   unsigned long long* err;
+};
+
+// Merge pass: every (token, kv head) whose key blocks were split over more
+// than one split-KV worker is merged from the workers' partials (and, in a
+// cascade, the prefix partials), after the split-KV grid. Each split-KV
+// worker w > 0 leaves the task of the slice boundary before it in tasks[w]:
+// {token, kv head, first worker, last worker} of the (token, kv head) that
+// boundary splits, if w is the first worker after its first boundary, else
+// token -1.
+struct MergeParams {
+  const WsHeader* header;
+  const int4* tasks;
+  const float* partials;
+  int slot_floats;
+  int num_workers;  // split-KV workers launched (the slicing's upper bound)
+  int num_q_heads, num_kv_heads, num_tokens;
+  int key_start_blocks;
+  const float* prefix_partials;
+  int prefix_chunks;
+  float v_scale;
+  uint16_t* out;
 };
 
 struct WriteParams {
@@ -228,7 +257,9 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
 // SMs x min(occupancy, occ_cap)).
 // f8 selects the E4M3-cache instantiation.
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool f8, int num_sms,
-                          int occ_cap, cudaStream_t s);
+                          int occ_cap, cudaStream_t s, int* workers_out);
+// The merge pass after a split-KV launch of num_workers workers (p.num_workers).
+cudaError_t launch_merge(const MergeParams& p, int head_dim, int group, cudaStream_t s);
 // Split-KV workers launch_decode will use on this device (0 on error).
 int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap);
 
@@ -242,7 +273,7 @@ int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap);
 #define PA_DEC_OCC_CAP_CASCADE 3
 #endif
 #ifndef PA_DEC_OCC_CAP_FP8
-#define PA_DEC_OCC_CAP_FP8 3  // E4M3 calls: smaller rings, a third CTA per SM
+#define PA_DEC_OCC_CAP_FP8 3  // E4M3 calls: smaller rings, a third CTA where registers allow
 #endif
 cudaError_t launch_prefill(const PrefillLaunch& a, int num_sms, cudaStream_t s);
 

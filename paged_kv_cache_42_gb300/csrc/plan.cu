@@ -8,12 +8,13 @@
 //    {token, request, keys to attend, first flattened position} with the
 //    prefix sum of Hkv * ceil(keys / 16) positions, which the split-KV
 //    kernel's workers slice into equal parts.
-//  - The merge counters of every (unit, kv head) are zeroed.
 //  - Cascade calls (common prefix of prefix_blocks blocks): every span goes
 //    to the split-KV path with the prefix blocks left out of its positions;
 //    requests must see the whole prefix and start with request 0's prefix
 //    blocks, which is checked here.
 // Invalid spans or lengths are skipped and reported on the device error word.
+// A decode-only batch needs no planner: the split-KV kernel builds its own
+// unit list.
 #include "pa_internal.h"
 #include "ptx.cuh"
 
@@ -53,10 +54,10 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 constexpr int kTileBuckets = 512;  // tiles sorted by key-tile count, longest first
 
 __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
-  // When the next grid has work that needs no plan (a self-planned split-KV
-  // grid, the cascade prefix pass), let it start now; a grid that would only
-  // wait at its top for the plan is released at the end of this one instead
-  // (starting it early measured slower).
+  // When the next grid has work that needs no plan (the cascade prefix
+  // pass), let it start now; a grid that would only wait at its top for the
+  // plan is released at the end of this one instead (starting it early
+  // measured slower).
   if (p.early_trigger) griddep_launch_dependents();
   __shared__ long long scan_sm[32];
   __shared__ int bucket_cnt[kTileBuckets];
@@ -66,20 +67,6 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   // workspace.
   extern __shared__ int2 dsm[];
   const int T = p.num_tokens;
-  if (p.self_plan) {
-    // a decode-only batch plans itself in the split-KV kernel; that kernel
-    // only needs its merge counters zeroed, before its first merge
-    for (long long i = threadIdx.x; i < (long long)T * p.num_kv_heads; i += blockDim.x)
-      p.counters[i] = 0;
-    if (threadIdx.x == 0) {
-      p.header->num_units = 0;
-      p.header->num_positions = 0;
-      p.header->num_tiles = 0;
-    }
-    if (!p.early_trigger) griddep_launch_dependents();
-    griddep_wait();  // complete only after the KV write (see the end of this kernel)
-    return;
-  }
   const bool in_smem = T <= kPlanSmemTokens;
   int2* const raw = in_smem ? dsm : p.raw;
   int* const ubase = in_smem ? reinterpret_cast<int*>(dsm + T) : nullptr;
@@ -183,8 +170,6 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     p.header->num_units = K;
     p.header->num_positions = W;
   }
-  for (long long i = threadIdx.x; i < (long long)T * p.num_kv_heads; i += blockDim.x)
-    p.counters[i] = 0;  // merge counters are per (token, kv head)
   // each split-KV worker's first unit (same worker count and slicing as the
   // split-KV kernel), found by binary search over the units' first positions
   if (ubase) {
@@ -229,9 +214,7 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   // A batch with no tensor-core work needs no bucket sort: a block sized to the
   // batch (fewer warps per barrier) plans it faster.
   int threads = kPlanThreads;
-  if (p.self_plan) {
-    threads = 256;
-  } else if (!p.use_prefill) {
+  if (!p.use_prefill) {
     const int need = p.num_tokens > p.num_reqs ? p.num_tokens : p.num_reqs;
     threads = need <= 128 ? 128 : need <= 256 ? 256 : need <= 512 ? 512 : kPlanThreads;
   }
