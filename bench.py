@@ -265,14 +265,17 @@ class Resident:
         self.h2d_bytes = self.h_pack.numel()  # copied per step (inputs plus alignment padding)
         self.d2h_bytes = self.out.numel() * self.out.element_size()
 
-    def step(self):
+    def step(self, out=None):
+        """One step (KV write, then attention) into `out` (the device output
+        unless given)."""
         d, w, b = self.d, self.w, self.binding
+        out = self.out if out is None else out
         if self.fp8:
             ks, vs = self.fp8
             b.write_kv_fp8(d["k"], d["v"], d["slot_mapping"], self.k_cache, self.v_cache, ks, vs)
             b.attention_fp8(d["q"], self.k_cache, self.v_cache, d["block_tables"], d["seq_lens"],
                             d["qsl"], w.scale, ks, vs, max_query_len=w.max_query_len,
-                            max_seq_len=w.max_seq_len, out=self.out, workspace=self.ws)
+                            max_seq_len=w.max_seq_len, out=out, workspace=self.ws)
             return
         b.write_kv(d["k"], d["v"], d["slot_mapping"], self.k_cache, self.v_cache)
         if self.cascade_len:
@@ -280,16 +283,18 @@ class Resident:
                                 d["seq_lens"], d["qsl"], w.scale,
                                 common_prefix_len=self.cascade_len,
                                 max_query_len=w.max_query_len, max_seq_len=w.max_seq_len,
-                                out=self.out, workspace=self.ws)
+                                out=out, workspace=self.ws)
         else:
             b.attention(d["q"], self.k_cache, self.v_cache, d["block_tables"], d["seq_lens"],
                         d["qsl"], w.scale, max_query_len=w.max_query_len,
-                        max_seq_len=w.max_seq_len, out=self.out, workspace=self.ws)
+                        max_seq_len=w.max_seq_len, out=out, workspace=self.ws)
 
     def step_e2e(self):
-        self.d_pack.copy_(self.h_pack, non_blocking=True)  # all of the step's inputs
-        self.step()
-        self.h_out.copy_(self.out, non_blocking=True)
+        # all of the step's inputs in one copy; the attention kernels store
+        # the result straight into pinned host memory (pa_mapped_pointer), so
+        # the device-to-host transfer overlaps the computation
+        self.d_pack.copy_(self.h_pack, non_blocking=True)
+        self.step(out=self.h_out)
 
 
 def workload_signature(w: wl.Workload) -> str:
@@ -563,7 +568,9 @@ def run_ours(args, rank, world, local, dist):
         res = main["res"]
         line["e2e"] = {"value": round(world * sb["step"] / (main["e2e_ms"] * 1e-3) / 1e9, 2),
                        "unit": "GB/s", "ms_per_step": round(main["e2e_ms"], 5),
-                       "h2d_bytes_per_step": res.h2d_bytes, "d2h_bytes_per_step": res.d2h_bytes}
+                       "h2d_bytes_per_step": res.h2d_bytes, "d2h_bytes_per_step": res.d2h_bytes,
+                       "path": "inputs: one copy from a pinned pack; output: stored by the "
+                               "kernels into pinned host memory (pa_mapped_pointer)"}
     if MIXED_CONFIG in result and MIXED_CONFIG != args.config:
         m = result[MIXED_CONFIG]
         mw = m["w"]

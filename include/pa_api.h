@@ -134,7 +134,10 @@ size_t pa_attention_workspace_size(int num_reqs, int num_tokens, int num_q_heads
  *   scale            multiplies q.k before the softmax (usually 1/sqrt(head_dim))
  *   out              [num_tokens][num_q_heads][head_dim] bf16; rows of
  *                    requests with qlen 0 and rows past query_start_loc[num_reqs]
- *                    are left untouched
+ *                    are left untouched. Device memory, or pinned host memory
+ *                    through the address pa_mapped_pointer gives: the kernels
+ *                    then store the result across the host link as they
+ *                    finish it, so no separate device-to-host copy follows.
  *   query head h reads KV head h / (num_q_heads / num_kv_heads)
  *   max_blocks_per_req  row stride of block_tables
  *   max_query_len, max_seq_len  host-side upper bounds the scheduler already
@@ -282,6 +285,15 @@ const char* pa_status_string(int status);
  * Either output pointer may be NULL.
  */
 pa_status pa_get_device_error(int* code, long long* detail, int clear);
+
+/*
+ * Device address of pinned host memory (cudaHostAlloc / cudaHostRegister,
+ * mapped into the device's address space): the address kernels use to reach
+ * it, which `out` of the attention calls accepts. PA_ERR_INVALID_ARG when
+ * host_ptr is not pinned host memory or device_ptr is NULL; PA_ERR_CUDA on a
+ * runtime error. *device_ptr is set only on success.
+ */
+pa_status pa_mapped_pointer(const void* host_ptr, void** device_ptr);
 
 /*
  * Instrumentation: record `start_event` / `stop_event` (cudaEvent_t handles

@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.pa_get_device_error.restype = _c_i
         L.pa_set_kernel_timer.argtypes = [_c_i, _c_p, _c_p]
         L.pa_set_kernel_timer.restype = _c_i
+        L.pa_mapped_pointer.argtypes = [_c_p, ctypes.POINTER(ctypes.c_void_p)]
+        L.pa_mapped_pointer.restype = _c_i
         L.pa_launch_count.argtypes = []
         L.pa_launch_count.restype = ctypes.c_longlong
         L.pa_version.argtypes = []
@@ -111,6 +113,25 @@ def _dev(t: torch.Tensor, dtype, name: str) -> int:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
+
+
+def _out(t: torch.Tensor) -> int:
+    """Address of an output tensor: a CUDA tensor, or a pinned CPU tensor
+    reached through its mapped device address (pa_mapped_pointer)."""
+    if isinstance(t, torch.Tensor) and not t.is_cuda:
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise TypeError("out must be a contiguous bf16 tensor")
+        if not t.is_pinned():
+            raise ValueError("a host out tensor must be pinned")
+        return mapped_pointer(t)
+    return _dev(t, torch.bfloat16, "out")
+
+
+def mapped_pointer(t: torch.Tensor) -> int:
+    """pa_mapped_pointer: the device address of a pinned host tensor."""
+    dp = ctypes.c_void_p()
+    _check(lib().pa_mapped_pointer(t.data_ptr(), ctypes.byref(dp)), "pa_mapped_pointer")
+    return int(dp.value)
 
 
 def status_string(status: int) -> str:
@@ -171,7 +192,7 @@ def attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
         _dev(seq_lens, torch.int32, "seq_lens"),
         _dev(query_start_loc, torch.int32, "query_start_loc"), float(scale),
-        _dev(out, torch.bfloat16, "out"), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+        _out(out), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
         int(max_query_len), int(max_seq_len), _dev(workspace, torch.uint8, "workspace"),
         int(workspace.numel()), _stream_ptr(stream))
     _check(st, "pa_attention")
@@ -220,7 +241,7 @@ def attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         _dev(v_cache, torch.uint8, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
         _dev(seq_lens, torch.int32, "seq_lens"),
         _dev(query_start_loc, torch.int32, "query_start_loc"), float(scale), float(k_scale),
-        float(v_scale), _dev(out, torch.bfloat16, "out"), R, T, hq, hkv, d, bs, nb,
+        float(v_scale), _out(out), R, T, hq, hkv, d, bs, nb,
         int(block_tables.shape[1]), int(max_query_len), int(max_seq_len),
         _dev(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream_ptr(stream))
     _check(st, "pa_attention_fp8")
@@ -257,7 +278,7 @@ def attention_cascade(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
         _dev(seq_lens, torch.int32, "seq_lens"),
         _dev(query_start_loc, torch.int32, "query_start_loc"), float(scale),
-        _dev(out, torch.bfloat16, "out"), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+        _out(out), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
         int(max_query_len), int(max_seq_len), int(common_prefix_len),
         _dev(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream_ptr(stream))
     _check(st, "pa_attention_cascade")
@@ -328,7 +349,7 @@ def attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
         _dev(seq_lens, torch.int32, "seq_lens"),
         _dev(query_start_loc, torch.int32, "query_start_loc"), float(scale),
-        _dev(out, torch.bfloat16, "out"), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
+        _out(out), R, T, hq, hkv, d, bs, nb, int(block_tables.shape[1]),
         int(max_query_len), int(max_seq_len), _stream_ptr(stream))
     _check(st, "pa_attention_noalloc")
     return out

@@ -97,21 +97,24 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
   }
   __syncthreads();
 
-  // combine the warps' shares (a warp without partials has m = -inf)
-  for (int e = threadIdx.x; e < G * D; e += kMergeWarps * 32) {
-    const int h = e / D, d = e - h * D;
+  // combine the warps' shares (a warp without partials has m = -inf), two
+  // output dims per thread, stored as one bf16 pair
+  for (int e = threadIdx.x; e < G * D / 2; e += kMergeWarps * 32) {
+    const int h = e / (D / 2), d = 2 * (e - h * (D / 2));
     float mx = -INFINITY;
 #pragma unroll
     for (int k = 0; k < kMergeWarps; ++k) mx = fmaxf(mx, s_m[k][h]);
-    float l = 0.f, o = 0.f;
+    float l = 0.f, o0 = 0.f, o1 = 0.f;
 #pragma unroll
     for (int k = 0; k < kMergeWarps; ++k) {
       const float f = s_m[k][h] == -INFINITY ? 0.f : exp2f(s_m[k][h] - mx);
       l += s_l[k][h] * f;
-      o += s_o[k][h][d] * f;
+      o0 += s_o[k][h][d] * f;
+      o1 += s_o[k][h][d + 1] * f;
     }
-    p.out[((size_t)tok * p.num_q_heads + (size_t)kv * G + h) * D + d] =
-        (uint16_t)(float2_to_bf16x2(o * (p.v_scale / l), 0.f) & 0xffffu);
+    const float sc = p.v_scale / l;
+    *reinterpret_cast<uint32_t*>(p.out + ((size_t)tok * p.num_q_heads + (size_t)kv * G + h) * D +
+                                 d) = float2_to_bf16x2(o0 * sc, o1 * sc);
   }
 }
 

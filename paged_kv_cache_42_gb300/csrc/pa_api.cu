@@ -433,6 +433,23 @@ pa_status pa_attention_cascade(const void* q, const void* k_cache, const void* v
                         common_prefix_len, 0, 1.f, 1.f, workspace, workspace_bytes, stream);
 }
 
+pa_status pa_mapped_pointer(const void* host_ptr, void** device_ptr) {
+  if (host_ptr == nullptr || device_ptr == nullptr) return PA_ERR_INVALID_ARG;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host_ptr) != cudaSuccess) {
+    cudaGetLastError();  // clear the error the query recorded
+    return PA_ERR_INVALID_ARG;
+  }
+  if (a.type != cudaMemoryTypeHost) return PA_ERR_INVALID_ARG;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, const_cast<void*>(host_ptr), 0) != cudaSuccess || !d) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  *device_ptr = d;
+  return PA_OK;
+}
+
 pa_status pa_get_device_error(int* code, long long* detail, int clear) {
   DeviceState* d = nullptr;
   if (pa_status st = device_state(&d)) return st;
