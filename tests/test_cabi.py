@@ -118,3 +118,14 @@ def test_device_calls_fail_cleanly_without_gpu(pa_lib):
     det = ctypes.c_longlong(0)
     assert pa_lib.pa_get_device_error(ctypes.byref(code), ctypes.byref(det), 0) == -4
     assert pa_lib.pa_init() == -4
+
+
+def test_mapped_pointer_rejects_null_arguments(pa_lib):
+    """pa_mapped_pointer checks its arguments before any CUDA call."""
+    f = pa_lib.pa_mapped_pointer
+    f.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+    f.restype = ctypes.c_int
+    out = ctypes.c_void_p(0)
+    assert f(None, ctypes.byref(out)) == -1
+    assert f(ctypes.c_void_p(FAKE), None) == -1
+    assert out.value is None
