@@ -8,6 +8,16 @@ the import-time loader raises.
 
 Function names follow the C ABI: ``pa_write_kv`` -> :func:`write_kv`,
 ``pa_attention`` -> :func:`attention`, and so on.
+
+The attention calls also take a pinned CPU tensor as ``out``. It is passed by
+its mapped device address (``pa_mapped_pointer``), and the kernels store the
+result straight into host memory. That overlaps the device-to-host transfer
+with the computation::
+
+    host_out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    attention(q, k_cache, v_cache, block_tables, seq_lens, qsl, scale,
+              max_query_len=1, max_seq_len=L, out=host_out)
+    torch.cuda.current_stream().synchronize()  # host_out now holds the result
 """
 from __future__ import annotations
 
