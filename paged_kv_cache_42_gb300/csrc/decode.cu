@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     K = p.header->num_units;
   }
   if (W <= 0) return;
-  const int NW = plan_workers(W, gridDim.x * WARPS);
+  const int launched = (int)gridDim.x * WARPS;
+  const int NW = plan_workers(W, launched < p.max_workers ? launched : p.max_workers);
   const int w = blockIdx.x * WARPS + warp;
   if (w >= NW) return;
   const int S = worker_begin(w, W, NW);

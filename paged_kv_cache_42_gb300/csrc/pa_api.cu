@@ -35,6 +35,8 @@ std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<long long> g_launches{0};
 std::atomic<int> g_self_plan{1};  // pa_set_option(PA_OPT_DECODE_SELF_PLAN, ...)
+std::atomic<int> g_decode_tc{1};  // pa_set_option(PA_OPT_DECODE_TC, ...): 0 off, 1 auto, 2 on
+std::atomic<int> g_max_workers{0};  // pa_set_option(PA_OPT_DECODE_MAX_WORKERS, ...): 0 = no cap
 constexpr int kNumTimers = 6;  // write, plan, decode, prefill, cascade prefix, merge
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
@@ -277,8 +279,17 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   pp.use_prefill = (prefix_len == 0 && max_query_len >= kPrefillMinQlen) ? 1 : 0;
   const int occ_cap =
       prefix_len > 0 ? PA_DEC_OCC_CAP_CASCADE : (kv_fp8 ? PA_DEC_OCC_CAP_FP8 : PA_DEC_OCC_CAP);
-  pp.num_workers = decode_workers(head_dim, pp.group, kv_fp8 != 0, d->num_sms, occ_cap);
-  if (pp.num_workers <= 0) return PA_ERR_CUDA;
+  // The tensor-core split-KV kernel takes the groups whose arithmetic per
+  // cached byte outgrows the CUDA cores (by default G >= PA_DECODE_TC_MIN_GROUP).
+  const int tc_mode = g_decode_tc.load();
+  const bool use_tc = tc_mode != 0 &&
+                      decode_tc_supported(head_dim, group, kv_fp8 != 0, prefix_len / kBlockSize) &&
+                      (tc_mode == 2 || group >= PA_DECODE_TC_MIN_GROUP);
+  const int launched = use_tc ? decode_tc_workers(d->num_sms)
+                              : decode_workers(head_dim, pp.group, kv_fp8 != 0, d->num_sms, occ_cap);
+  if (launched <= 0) return PA_ERR_CUDA;
+  const int cap = g_max_workers.load();
+  pp.num_workers = (cap > 0 && cap < launched) ? cap : launched;
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
   pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
   pp.tiles = reinterpret_cast<PrefillTile*>(ws + lay.tiles_off);
@@ -354,15 +365,20 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   dp.seq_lens = seq_lens;
   dp.header_out = pp.header;
   dp.merge_tasks = reinterpret_cast<int4*>(ws + lay.tasks_off);
+  dp.max_workers = cap > 0 ? cap : kMaxDecodeWorkers;
   dp.err = d->err;
-  int workers = 0;
+  int launched_workers = 0;
   {
     TimerScope timer(2, s);
-    const cudaError_t e = launch_decode(dp, head_dim, group, kv_fp8 != 0, d->num_sms, occ_cap, s,
-                                        &workers);
+    const cudaError_t e =
+        use_tc ? launch_decode_tc(dp, group, d->num_sms, s, &launched_workers)
+               : launch_decode(dp, head_dim, group, kv_fp8 != 0, d->num_sms, occ_cap, s,
+                               &launched_workers);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
+  // the slicing's worker count, as the split-KV kernel computes it
+  const int workers = (cap > 0 && cap < launched_workers) ? cap : launched_workers;
 
   MergeParams mp;
   mp.header = pp.header;
@@ -468,6 +484,14 @@ pa_status pa_set_option(int option, int value) {
   switch (option) {
     case PA_OPT_DECODE_SELF_PLAN:
       g_self_plan.store(value ? 1 : 0);
+      return PA_OK;
+    case PA_OPT_DECODE_TC:
+      if (value < 0 || value > 2) return PA_ERR_INVALID_ARG;
+      g_decode_tc.store(value);
+      return PA_OK;
+    case PA_OPT_DECODE_MAX_WORKERS:
+      if (value < 0) return PA_ERR_INVALID_ARG;
+      g_max_workers.store(value);
       return PA_OK;
   }
   return PA_ERR_INVALID_ARG;

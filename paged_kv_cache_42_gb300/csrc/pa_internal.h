@@ -206,6 +206,9 @@ struct DecodeParams {
   WsHeader* header_out;
   // merge task of the slice boundary before each worker (see MergeParams)
   int4* merge_tasks;
+  // workers the slicing uses: at most the launched ones (a smaller value
+  // leaves the rest idle and gives every worker a longer slice)
+  int max_workers;
   unsigned long long* err;
 };
 
@@ -263,6 +266,21 @@ cudaError_t launch_merge(const MergeParams& p, int head_dim, int group, cudaStre
 // Split-KV workers launch_decode will use on this device (0 on error).
 int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap);
 
+// Tensor-core split-KV decode (decode_tc.cu): one CTA per SM is one worker.
+// Supported for head_dim 128 over a bf16 cache without a cascade prefix; it
+// takes the same plan, partial slots and merge tasks as launch_decode.
+bool decode_tc_supported(int head_dim, int group, bool f8, int key_start_blocks);
+int decode_tc_workers(int num_sms);
+cudaError_t launch_decode_tc(const DecodeParams& p, int group, int num_sms, cudaStream_t s,
+                             int* workers_out);
+
+// 2-D tiled tensor map (CUtensorMap, passed as void*) over a row-major bf16
+// matrix of `rows` rows of `inner` elements, `row_stride_bytes` apart, with a
+// {box_inner, box_rows} box and 128-byte swizzle. False if the driver's
+// encoder is unavailable or rejects the arguments.
+bool encode_tmap_bf16_2d(void* tmap, const void* ptr, uint64_t inner, uint64_t rows,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+
 // Resident split-KV CTAs per SM: two suit long per-token key ranges (each
 // worker's slice stays long); the short suffixes of a cascade call run better
 // with a third, which hides more latency.
@@ -271,6 +289,10 @@ int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap);
 #endif
 #ifndef PA_DEC_OCC_CAP_CASCADE
 #define PA_DEC_OCC_CAP_CASCADE 3
+#endif
+// Smallest GQA group the tensor-core split-KV kernel takes in automatic mode.
+#ifndef PA_DECODE_TC_MIN_GROUP
+#define PA_DECODE_TC_MIN_GROUP 8
 #endif
 #ifndef PA_DEC_OCC_CAP_FP8
 #define PA_DEC_OCC_CAP_FP8 3  // E4M3 calls: smaller rings, a third CTA where registers allow

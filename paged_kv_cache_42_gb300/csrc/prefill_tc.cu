@@ -726,6 +726,19 @@ bool encode_bf16(CUtensorMap* m, int rank, const void* ptr, const cuuint64_t* di
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool encode_tmap_bf16_2d(void* tmap, const void* ptr, uint64_t inner, uint64_t rows,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+  if (!get_encoder()) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t str[1] = {(cuuint64_t)row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  return encode_bf16(static_cast<CUtensorMap*>(tmap), 2, ptr, dims, str, box);
+}
+
+namespace {
+
 template <int D, int G, bool PREFIX, bool F8>
 cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s) {
   using C = PCfg<D, G>;
