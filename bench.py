@@ -49,6 +49,7 @@ METRIC = "paged-attn decode KV GB/s (frac of HBM peak); mixed-batch tokens/s per
 HEADLINE_CONFIG = 2
 MIXED_CONFIG = 3
 PREFIX_CONFIG = 4
+LONG_CONFIG = 5
 FP8_SCALES = (0.0113, 0.0127)  # k_scale, v_scale of the E4M3 cache runs
 FALLBACK_HBM_GBS = 6800.0
 
@@ -96,22 +97,49 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "of fallback"}
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken with the decode kernel source as it is now; else None."""
+# The split-KV kernel a bf16 call routes to (the library's default routing):
+# the tensor-core kernel for groups of 8 query heads per KV head at head_dim
+# 128, the CUDA-core kernel otherwise.
+def split_kv_kernel(w: wl.Workload, fp8: bool = False, cascade: bool = False) -> tuple:
+    g = w.num_q_heads // w.num_kv_heads
+    if w.head_dim == 128 and g >= 8 and not fp8 and not cascade:
+        return "pa_decode_tc_kernel", "decode_tc.cu"
+    return "pa_decode_kernel", "decode.cu"
+
+
+def ncu_traffic(workload: str, src_name: str = "decode.cu"):
+    """DRAM bytes per split-KV launch from the committed ncu summary, if it
+    was taken with that kernel's source as it is now; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    src = os.path.join(ROOT, "paged_kv_cache_42_gb300", "csrc", "decode.cu")
+    src = os.path.join(ROOT, "paged_kv_cache_42_gb300", "csrc", src_name)
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         e = d.get(workload)
-        if e and e.get("decode_cu_sha") == sha:
+        if e and e.get("source_sha", e.get("decode_cu_sha")) == sha and \
+                e.get("source", "decode.cu") == src_name:
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
     return None
+
+
+# The pages' own figures, quoted as context (system-level; none is a target
+# and none was measured on this hardware).
+PAGES_CONTEXT = [
+    {"figure": "2-4x serving throughput over FasterTransformer and Orca at comparable latency",
+     "hardware": "not stated on the pages",
+     "source": "Deep Dive - vLLM (leetllm), introduction; Inside the vLLM Engine, "
+               "'A memory problem wearing a throughput costume'"},
+    {"figure": "20.4-38.2% of KV-cache memory holds token state in prior systems",
+     "hardware": "not stated on the pages",
+     "source": "Inside the vLLM Engine, 'A memory problem wearing a throughput costume'"},
+    {"figure": "under 4% of KV memory wasted with paging (60-80% in prior systems)",
+     "hardware": "not stated on the pages",
+     "source": "vLLM: An Exhaustive Technical Study for Kernel Engineers, 2.1"},
+]
 
 
 # ---------------------------------------------------------------------------
@@ -437,6 +465,33 @@ def fp8_timing(args, flush, torch, binding, dist, rank, world, peaks) -> dict:
             "requests_per_s": round(world * w.num_reqs / (ms * 1e-3), 1)}
 
 
+def long_context_timing(args, flush, torch, binding, dist, rank, world, peaks) -> dict:
+    """The long-context decode batch (8 x 32768 tokens, 64 query / 8 KV heads):
+    the split-KV showcase, on the kernel the library routes it to."""
+    w = wl.make_config(LONG_CONFIG, seed=42 + LONG_CONFIG + 1000 * rank)
+    sb = step_bytes(w)
+    steps = max(50, args.steps // 10)
+    res = Resident(w, torch, binding)
+    t = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
+    tk = time_kernels(res, steps, args.warmup, flush, torch, binding, dist)
+    code, detail = binding.get_device_error(clear=True)
+    if code:
+        raise RuntimeError(f"device error {code} at {detail}")
+    ms = max_over_ranks(t["ms_per_step"], dist)
+    dec = tk["decode_ms"]
+    del res
+    torch.cuda.empty_cache()
+    kname, ksrc = split_kv_kernel(w)
+    achieved = sb["attention"] / (dec * 1e-3) / 1e9
+    return {"workload": f"{wl.CONFIG_NAMES[LONG_CONFIG]}: {wl.CONFIG_DESCRIPTIONS[LONG_CONFIG]}",
+            "steps": steps, "ms_per_step": round(ms, 5), "kernel": kname,
+            "decode_kernel_ms": round(dec, 5), "algorithmic_bytes_per_launch": sb["attention"],
+            "achieved_gbs": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
+            "traffic": ncu_traffic(wl.CONFIG_NAMES[LONG_CONFIG], ksrc),
+            "step_gbs": round(world * sb["step"] / (ms * 1e-3) / 1e9, 1)}
+
+
 def graph_steps(res: Resident, steps: int, warmup: int, flush, torch, dist) -> float:
     """ms per step when the step's calls (write + attention) are captured once
     in a CUDA graph and replayed; the L2 flush stays outside the timed region."""
@@ -525,6 +580,7 @@ def run_ours(args, rank, world, local, dist):
     main = result[args.config]
     w, sb = main["w"], main["sb"]
     ms = main["ms"]
+    kname, ksrc = split_kv_kernel(w, fp8=bool(args.fp8), cascade=bool(args.cascade))
     value = world * sb["step"] / (ms * 1e-3) / 1e9
     achieved = sb["attention"] / (main["dec_ms"] * 1e-3) / 1e9
     line = {
@@ -547,10 +603,10 @@ def run_ours(args, rank, world, local, dist):
                    "l2": "flushed before every timed step (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {
-            "bound": "hbm", "kernel": "pa_decode_kernel",
+            "bound": "hbm", "kernel": kname,
             "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-            "traffic": ncu_traffic(wl.CONFIG_NAMES[args.config]),
+            "traffic": ncu_traffic(wl.CONFIG_NAMES[args.config], ksrc),
             "algorithmic_bytes_per_launch": sb["attention"],
             "kernel_ms": round(main["dec_ms"], 5)},
         "gpu_launches": int(main["t"]["launches"]),
@@ -588,8 +644,12 @@ def run_ours(args, rank, world, local, dist):
             "kv_bytes": m["sb"]["kv"], "prefill_causal_flops": prefill_flops(mw)}
     if not args.quick and args.config != PREFIX_CONFIG:
         line["prefix_share"] = prefix_share_timing(args, flush, torch, binding, dist, rank, world)
+    if not args.quick and args.config != LONG_CONFIG:
+        line["long_context"] = long_context_timing(args, flush, torch, binding, dist, rank, world,
+                                                   peaks)
     if not args.quick:
         line["kv_fp8"] = fp8_timing(args, flush, torch, binding, dist, rank, world, peaks)
+    line["pages_context"] = PAGES_CONTEXT
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0 and not args.quick:

@@ -178,13 +178,17 @@ pa_status pa_write_kv_fp8(const void* k, const void* v, const int64_t* slot_mapp
 
 /*
  * pa_attention_fp8: pa_attention over E4M3 caches written by pa_write_kv_fp8.
- * Keys are value(code) * k_scale and values value(code) * v_scale; the
- * dequantisation is fused into the split-KV kernel (codes widen exactly to
- * fp32; k_scale is folded into the query scaling and v_scale into the output).
- * Every span runs on the split-KV kernel: prefill chunks do not take the
- * tensor-core path over an FP8 cache. The workspace is
- * pa_attention_workspace_size(...) bytes, as for pa_attention. Errors as
- * pa_attention, plus PA_ERR_INVALID_ARG for a scale that is not finite and > 0.
+ * Keys are value(code) * k_scale and values value(code) * v_scale, and the
+ * dequantisation is fused into both attention kernels, as for a bf16 cache:
+ *  - prefill chunks (spans of 16 or more new tokens) run on the tensor-core
+ *    kernel, whose converter warps widen each E4M3 tile exactly to bf16 in
+ *    shared memory before the bf16 MMA;
+ *  - every other span (decodes, short spans) runs on the CUDA-core split-KV
+ *    kernel, which widens codes exactly to fp32.
+ * k_scale is folded into the query scaling and v_scale into the output. The
+ * workspace is pa_attention_workspace_size(...) bytes, as for pa_attention.
+ * Errors as pa_attention, plus PA_ERR_INVALID_ARG for a scale that is not
+ * finite and > 0.
  */
 pa_status pa_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
                            const int32_t* block_tables, const int32_t* seq_lens,
@@ -253,9 +257,14 @@ pa_status pa_attention_cascade(const void* q, const void* k_cache, const void* v
  *  - A batch whose pa_attention_workspace_size(...) exceeds
  *    PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_WORKSPACE before
  *    anything is launched.
+ *  - Argument errors are reported as pa_attention reports them (the same
+ *    codes, checked first), whatever the batch size; the size check follows.
  *  - The first call on a device looks up the scratch array's device address
- *    (with that device current); make that first call before any stream
- *    capture.
+ *    (with that device current). With lazy module loading (the CUDA default)
+ *    that lookup is also when the driver places the array in device memory:
+ *    an allocation the driver makes once, on that first call. So make the
+ *    first call on each device outside any context that must not allocate,
+ *    and before any stream capture; later calls allocate nothing.
  *  - Every call on a device shares the one scratch array, which keeps the
  *    last call's contents; the kernels re-initialise everything they read
  *    from it on each call. Calls whose work overlaps on the GPU (different
@@ -283,6 +292,12 @@ const char* pa_status_string(int status);
  * *detail the offending index (token, request or block position). With
  * clear != 0 the word is reset. Synchronises the device; not for the hot path.
  * Either output pointer may be NULL.
+ * There is one error word per device, in the library's static device memory,
+ * shared by every call on that device whatever its stream: the first error
+ * recorded since the last clear wins, so calls running concurrently on
+ * different streams cannot tell whose error it is, and a clear resets it for
+ * all of them. (The word's address is cached at the first call on a device;
+ * the library does not support cudaDeviceReset of a device it has used.)
  */
 pa_status pa_get_device_error(int* code, long long* detail, int clear);
 

@@ -352,8 +352,14 @@ def attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                        _c_i, _c_p]
     L.pa_attention_noalloc.restype = _c_i
     T, hq, d = q.shape
-    nb, hkv, bs, _ = k_cache.shape
+    nb, hkv, bs, d2 = k_cache.shape
     R = int(seq_lens.shape[0])
+    if d2 != d or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between q and the caches")
+    if query_start_loc.shape != (R + 1,) or block_tables.dim() != 2 or block_tables.shape[0] != R:
+        raise ValueError("metadata shapes must be qsl [R+1], block_tables [R, max_blocks]")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
     st = L.pa_attention_noalloc(
         _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
         _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),

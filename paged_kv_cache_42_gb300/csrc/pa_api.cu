@@ -25,8 +25,11 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Per-device set-up, done once. The cached device address of the error word
+// stays valid for the life of the CUDA context: the library does not support
+// cudaDeviceReset of a device it has been used on.
 struct DeviceState {
-  bool ready = false;
+  std::atomic<bool> ready{false};
   int num_sms = 0;
   unsigned long long* err = nullptr;
 };
@@ -47,9 +50,9 @@ pa_status device_state(DeviceState** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
   DeviceState& d = g_devices[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       int sms = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PA_ERR_CUDA;
@@ -57,7 +60,7 @@ pa_status device_state(DeviceState** out) {
       if (cudaGetSymbolAddress(&err, g_device_error) != cudaSuccess) return PA_ERR_CUDA;
       d.num_sms = sms;
       d.err = static_cast<unsigned long long*>(err);
-      d.ready = true;
+      d.ready.store(true, std::memory_order_release);
     }
   }
   *out = &d;
@@ -85,6 +88,50 @@ struct TimerScope {
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 
 }  // namespace
+
+pa_status check_attention_args(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, float scale, const void* out,
+                               int num_reqs, int num_tokens, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_req, int max_query_len, int max_seq_len,
+                               int prefix_len, int kv_fp8, float k_scale, float v_scale,
+                               bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (kv_fp8 && !(k_scale > 0.f && k_scale < INFINITY && v_scale > 0.f && v_scale < INFINITY))
+    return PA_ERR_INVALID_ARG;
+  if (kv_fp8 && prefix_len > 0) return PA_ERR_UNSUPPORTED;  // no FP8 cascade
+  if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      head_dim <= 0 || num_blocks < 0 || max_blocks_per_req < 0 || max_query_len < 0 ||
+      max_seq_len < 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128) ||
+      !supported_group(num_q_heads / num_kv_heads))
+    return PA_ERR_UNSUPPORTED;
+  if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN scale
+  if (num_reqs == 0 || num_tokens == 0) {
+    *nothing_to_do = true;
+    return PA_OK;
+  }
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
+    return PA_ERR_INVALID_ARG;
+  // flattened work positions must fit a 32-bit int: tokens x Hkv x blocks per token
+  const long long max_blocks = ((long long)max_seq_len + kBlockSize - 1) / kBlockSize;
+  if ((long long)num_tokens * num_kv_heads * max_blocks >= (1LL << 31))
+    return PA_ERR_UNSUPPORTED;
+  // a cascade prefix is whole blocks, inside the tables, and leaves every
+  // request at least one key of its own
+  if (prefix_len > 0 && (prefix_len / kBlockSize > max_blocks_per_req || prefix_len >= max_seq_len))
+    return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -203,34 +250,14 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
                          int max_query_len, int max_seq_len, int prefix_len, int kv_fp8,
                          float k_scale, float v_scale, void* workspace,
                          size_t workspace_bytes, void* stream) {
-  if (kv_fp8 && !(k_scale > 0.f && k_scale < INFINITY && v_scale > 0.f && v_scale < INFINITY))
-    return PA_ERR_INVALID_ARG;
-  if (kv_fp8 && prefix_len > 0) return PA_ERR_UNSUPPORTED;  // no FP8 cascade
-  if (num_reqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-      head_dim <= 0 || num_blocks < 0 || max_blocks_per_req < 0 || max_query_len < 0 ||
-      max_seq_len < 0)
-    return PA_ERR_INVALID_ARG;
-  if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
-  if (block_size != kBlockSize || (head_dim != 64 && head_dim != 128) ||
-      !supported_group(num_q_heads / num_kv_heads))
-    return PA_ERR_UNSUPPORTED;
-  if (!(scale == scale)) return PA_ERR_INVALID_ARG;  // NaN scale
-  if (num_reqs == 0 || num_tokens == 0) return PA_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
-    return PA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
-      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
-      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
-    return PA_ERR_INVALID_ARG;
-  // flattened work positions must fit a 32-bit int: tokens x Hkv x blocks per token
-  const long long max_blocks = ((long long)max_seq_len + kBlockSize - 1) / kBlockSize;
-  if ((long long)num_tokens * num_kv_heads * max_blocks >= (1LL << 31))
-    return PA_ERR_UNSUPPORTED;
-  // a cascade prefix is whole blocks, inside the tables, and leaves every
-  // request at least one key of its own
-  if (prefix_len > 0 && (prefix_len / kBlockSize > max_blocks_per_req || prefix_len >= max_seq_len))
-    return PA_ERR_INVALID_ARG;
+  bool nothing = false;
+  if (pa_status st = check_attention_args(
+          q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out, num_reqs,
+          num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+          max_blocks_per_req, max_query_len, max_seq_len, prefix_len, kv_fp8, k_scale, v_scale,
+          &nothing))
+    return st;
+  if (nothing) return PA_OK;
   const WsLayout lay = ws_layout(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim);
   const size_t need =
       lay.total + (prefix_len > 0

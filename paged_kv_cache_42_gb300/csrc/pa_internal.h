@@ -252,6 +252,19 @@ __device__ inline void report_error(unsigned long long* err, int code, long long
     atomicExch(err + 1, (unsigned long long)detail);
 }
 
+// Host-side checks of an attention call's arguments, everything but the
+// workspace (shapes, supported sizes, pointers, alignment, index ranges), in
+// the order pa_attention reports them. *nothing_to_do is set for an empty
+// batch (no request or no token), which is not an error.
+pa_status check_attention_args(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, float scale, const void* out,
+                               int num_reqs, int num_tokens, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks,
+                               int max_blocks_per_req, int max_query_len, int max_seq_len,
+                               int prefix_len, int kv_fp8, float k_scale, float v_scale,
+                               bool* nothing_to_do);
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_write_kv(const WriteParams& p, cudaStream_t s);
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);

@@ -14,6 +14,10 @@
 // Nothing here allocates: no cudaMalloc / cudaFree, no library allocator.
 // The array's device address is looked up once per device (with that device
 // current) and then handed to the unchanged pa_attention as its workspace.
+// With lazy module loading, that first lookup is also when the driver places
+// the array in device memory, so the first call on a device belongs outside
+// any context that must not allocate. The cached address is valid for the
+// life of the CUDA context (cudaDeviceReset is not supported).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -63,6 +67,14 @@ pa_status pa_attention_noalloc(const void* q, const void* k_cache, const void* v
                                int head_dim, int block_size, int num_blocks,
                                int max_blocks_per_req, int max_query_len, int max_seq_len,
                                void* stream) {
+  // argument errors first, as pa_attention reports them, whatever the batch size
+  bool nothing = false;
+  if (pa_status st = pa::check_attention_args(
+          q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale, out, num_reqs,
+          num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+          max_blocks_per_req, max_query_len, max_seq_len, 0, 0, 1.f, 1.f, &nothing))
+    return st;
+  if (nothing) return PA_OK;
   const size_t need =
       pa_attention_workspace_size(num_reqs, num_tokens, num_q_heads, num_kv_heads, head_dim);
   if (need == 0) return PA_ERR_INVALID_ARG;

@@ -129,3 +129,24 @@ def test_mapped_pointer_rejects_null_arguments(pa_lib):
     assert f(None, ctypes.byref(out)) == -1
     assert f(ctypes.c_void_p(FAKE), None) == -1
     assert out.value is None
+
+
+def noalloc(pa_lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, qsl=FAKE, scale=0.125, out=FAKE, R=4,
+             T=4, hq=4, hkv=2, d=64, bs=16, nb=32, mb=4, mq=1, ms=56)
+    a.update(kw)
+    return pa_lib.pa_attention_noalloc(a["q"], a["kc"], a["vc"], a["bt"], a["sl"], a["qsl"],
+                                       ctypes.c_float(a["scale"]), a["out"], a["R"], a["T"],
+                                       a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["mb"],
+                                       a["mq"], a["ms"], None)
+
+
+def test_noalloc_reports_argument_errors_before_the_size_check(pa_lib):
+    """A batch too large for the fixed scratch still gets pa_attention's own
+    error code when its arguments are wrong (checked on the host, no GPU)."""
+    big = dict(R=1 << 19, T=1 << 19, hq=32, hkv=8, d=128, ms=16)
+    assert noalloc(pa_lib, **big) == -3                # well-formed but too large
+    assert noalloc(pa_lib, **dict(big, d=96)) == -2    # unsupported head_dim
+    assert noalloc(pa_lib, **dict(big, q=None)) == -1  # null pointer
+    assert noalloc(pa_lib, **dict(big, bs=32)) == -2   # unsupported block size
+    assert noalloc(pa_lib, R=0) == 0                   # empty batch: nothing to do
