@@ -98,11 +98,15 @@ def measured_peaks() -> dict:
 
 
 # The split-KV kernel a bf16 call routes to (the library's default routing):
-# the tensor-core kernel for groups of 8 query heads per KV head at head_dim
-# 128, the CUDA-core kernel otherwise.
-def split_kv_kernel(w: wl.Workload, fp8: bool = False, cascade: bool = False) -> tuple:
+# the tensor-core kernel for groups of 4 or 8 query heads per KV head at
+# head_dim 128, the CUDA-core kernel otherwise.
+def split_kv_kernel(w: wl.Workload, fp8: bool = False, cascade: bool = False,
+                    force: str = "auto") -> tuple:
     g = w.num_q_heads // w.num_kv_heads
-    if w.head_dim == 128 and g >= 8 and not fp8 and not cascade:
+    tc_ok = w.head_dim == 128 and not fp8 and not cascade
+    if force == "cuda-core" or not tc_ok:
+        return "pa_decode_kernel", "decode.cu"
+    if force == "tensor-core" or g >= 4:
         return "pa_decode_tc_kernel", "decode_tc.cu"
     return "pa_decode_kernel", "decode.cu"
 
@@ -481,7 +485,7 @@ def long_context_timing(args, flush, torch, binding, dist, rank, world, peaks) -
     dec = tk["decode_ms"]
     del res
     torch.cuda.empty_cache()
-    kname, ksrc = split_kv_kernel(w)
+    kname, ksrc = split_kv_kernel(w, force=args.split_kv)
     achieved = sb["attention"] / (dec * 1e-3) / 1e9
     return {"workload": f"{wl.CONFIG_NAMES[LONG_CONFIG]}: {wl.CONFIG_DESCRIPTIONS[LONG_CONFIG]}",
             "steps": steps, "ms_per_step": round(ms, 5), "kernel": kname,
@@ -533,6 +537,7 @@ def run_ours(args, rank, world, local, dist):
     torch.cuda.set_device(local)
     binding.init()
     binding.get_device_error(clear=True)
+    binding.set_option("decode_tc", {"auto": 1, "cuda-core": 0, "tensor-core": 2}[args.split_kv])
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
@@ -580,7 +585,8 @@ def run_ours(args, rank, world, local, dist):
     main = result[args.config]
     w, sb = main["w"], main["sb"]
     ms = main["ms"]
-    kname, ksrc = split_kv_kernel(w, fp8=bool(args.fp8), cascade=bool(args.cascade))
+    kname, ksrc = split_kv_kernel(w, fp8=bool(args.fp8), cascade=bool(args.cascade),
+                                  force=args.split_kv)
     value = world * sb["step"] / (ms * 1e-3) / 1e9
     achieved = sb["attention"] / (main["dec_ms"] * 1e-3) / 1e9
     line = {
@@ -599,6 +605,7 @@ def run_ours(args, rank, world, local, dist):
         "config": {"workload": f"{wl.CONFIG_NAMES[args.config]}: "
                                f"{wl.CONFIG_DESCRIPTIONS[args.config]}",
                    "num_reqs": w.num_reqs, "num_tokens": w.num_tokens,
+                   "split_kv": args.split_kv,
                    "step_signature": main["signature"],
                    "l2": "flushed before every timed step (2x L2 written, then 2x L2 read)",
                    "parallelism": f"replicas x{world}"},
@@ -787,6 +794,9 @@ def main():
     ap.add_argument("--cascade", action="store_true",
                     help="step the chosen workload through pa_attention_cascade (its shared "
                          "prefix as the common prefix; the prefix-sharing workload has one)")
+    ap.add_argument("--split-kv", choices=["auto", "cuda-core", "tensor-core"], default="auto",
+                    help="split-KV kernel: the library's routing (default), or one forced "
+                         "(pa_set_option PA_OPT_DECODE_TC 0 / 2)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

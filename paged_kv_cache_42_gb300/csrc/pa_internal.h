@@ -293,6 +293,11 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int group, int num_sms, cuda
 // encoder is unavailable or rejects the arguments.
 bool encode_tmap_bf16_2d(void* tmap, const void* ptr, uint64_t inner, uint64_t rows,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+// Tiled tensor map of `rank` (<= 5) dimensions over bf16 data: dims[0] is
+// contiguous; strides_bytes[i] is the byte stride of dimension i + 1 (any
+// order: a dimension may step inside another's extent); 128-byte swizzle.
+bool encode_tmap_bf16(void* tmap, int rank, const void* ptr, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box);
 
 // Resident split-KV CTAs per SM: two suit long per-token key ranges (each
 // worker's slice stays long); the short suffixes of a cascade call run better
@@ -304,8 +309,12 @@ bool encode_tmap_bf16_2d(void* tmap, const void* ptr, uint64_t inner, uint64_t r
 #define PA_DEC_OCC_CAP_CASCADE 3
 #endif
 // Smallest GQA group the tensor-core split-KV kernel takes in automatic mode.
+// From 4 query heads per KV head it is at least as fast per step as the
+// CUDA-core kernel (equal on the Llama-8B decode batch, faster on the mixed,
+// prefix-sharing and long-context batches); below, the CUDA cores are not
+// short of arithmetic.
 #ifndef PA_DECODE_TC_MIN_GROUP
-#define PA_DECODE_TC_MIN_GROUP 8
+#define PA_DECODE_TC_MIN_GROUP 4
 #endif
 #ifndef PA_DEC_OCC_CAP_FP8
 #define PA_DEC_OCC_CAP_FP8 3  // E4M3 calls: smaller rings, a third CTA where registers allow
