@@ -59,6 +59,25 @@
 // and the q rows of the tile's portions). Block ids are loaded two tiles
 // ahead of their use.
 //
+// E4M3 caches (the F8 instantiation; "vLLM: An Exhaustive Technical Study for
+// Kernel Engineers", 2.8: E4M3 codes with per-tensor k_scale / v_scale). Both
+// products run as tcgen05.mma kind::f8f6f4 straight on the cached codes, so
+// nothing widens K or V:
+//   S^T = K Q'^T     each query row q is scaled by a power of two 2^e that
+//                    brings its largest magnitude into [128, 256) and split
+//                    into two E4M3 terms, q 2^e = hi + lo (exact for every
+//                    element within 2^9 of the row's largest), by a small
+//                    kernel before this one (launch_qsplit). N = 32: per slot,
+//                    8 rows of hi then 8 of lo; the softmax adds the two
+//                    column groups and undoes 2^e.
+//   O^T += V^T P'^T  P' = 256 p against a reference max that moves whenever
+//                    a tile's max exceeds it by more than 0.75 (so P' <= 430,
+//                    inside E4M3's 448), split the same way into hi + lo (a
+//                    relative error near 2^-8, as bf16's); O^T keeps the two
+//                    column groups apart until the epilogue.
+// An E4M3 block is one 2 KB copy per tensor ([16 keys][128 B] rows are
+// already the swizzle width), a stage 37 KB, five stages.
+//
 // Warp roles (192 threads, one CTA per SM): warps 0-3 softmax and epilogue
 // (warp w reads TMEM lanes 32w .. 32w+31), warp 4 the TMA producer (it also
 // walks the work list and publishes a record per tile), warp 5 allocates TMEM
@@ -81,38 +100,78 @@ namespace {
 
 constexpr unsigned kAllLanes = 0xffffffffu;
 constexpr int kD = 128;                   // head dim of this kernel
-constexpr int kStages = 3;
 constexpr int kTileBlocks = 8;            // 16-key cache blocks per 128-key tile
-// A K or V tile (128 keys x 128 dims) in shared memory: 16 groups of 8 keys,
-// 2 KB apart; in a group, the 64-dim half h 1 KB in, as 8 rows of 128 B
-// (128B-swizzled). One TMA copy lands a 16-key block: 2 groups x 2 halves.
-constexpr int kGroup = 2048;              // stride of 8-key groups
-constexpr int kHalfOff = 1024;            // offset of the second 64-dim half in a group
-constexpr int kKvTile = 16 * kGroup;      // K (or V) of one tile: 32 KB
-constexpr int kNhalf = 16 * 128;          // one half of a 16-row N operand (q rows, P^T)
-constexpr int kNbuf = 2 * kNhalf;
 constexpr int kWarps = 6;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kTmemCols = 64;             // S (2 x 16 columns), O (16 columns)
-constexpr uint32_t kTmS = 0, kTmO = 32;
 
-// Shared memory, from a 1024-byte aligned base. A stage holds one 128-key
-// tile: K, V, and the q rows of the (at most two) portions it covers.
-constexpr int kQBytes = 2 * kNhalf;            // q rows: [2 slots][2 halves][8 rows][128 B]
-constexpr int kStageBytes = 2 * kKvTile + kQBytes;
-constexpr int OFF_STAGE = 0;
-constexpr int OFF_P = kStages * kStageBytes;   // 2 buffers of P^T
-constexpr int OFF_REC = OFF_P + 2 * kNbuf;     // one tile record per stage
-constexpr int OFF_XCH = OFF_REC + kStages * 64;  // [2][4 warps][16] floats
-enum : int {
-  B_FULL = 0 /* x3 */, B_EMPTY = 3 /* x3 */, B_S = 6 /* x2 */, B_PREADY = 8 /* x2 */,
-  B_PFREE = 10 /* x2 */, B_XCH = 12 /* x2 */, B_DRAIN = 14, B_COUNT = 15
+// Shared-memory and TMEM layout of each instantiation, from a 1024-byte
+// aligned base. A stage holds one 128-key tile: K, V, and the query operand
+// rows of the (at most two) portions it covers.
+template <bool F8>
+struct TcL;
+// bf16 cache. A K or V tile (128 keys x 128 dims): 16 groups of 8 keys, 2 KB
+// apart; in a group, the 64-dim half h 1 KB in, as 8 rows of 128 B
+// (128B-swizzled). One TMA copy lands a 16-key block: 2 groups x 2 halves.
+// The q operand: [2 slots][2 halves][8 rows][128 B]; P^T: [2 key halves][16
+// rows][128 B]. N = 16: slot s is rows / columns 8 s .. 8 s + 7.
+template <>
+struct TcL<false> {
+  static constexpr int kStages = 3;
+  static constexpr int kGroup = 2048;      // K operand: stride of 8-row groups (SBO)
+  static constexpr int kHalfOff = 1024;    // second 64-dim half within a group
+  static constexpr int kKvTile = 32768;
+  static constexpr int kQBytes = 4096;
+  static constexpr int kN = 16;            // MMA N, columns of S^T and O^T
+  static constexpr int kSlotCols = 8;      // columns of one slot
+  static constexpr int kKStep = 16;        // MMA K per instruction (elements)
+  static constexpr int kPBytes = 4096;
+  static constexpr uint32_t kTmemCols = 64;
 };
-constexpr int OFF_BAR = OFF_XCH + 2 * 4 * 16 * 4;
-constexpr int OFF_TSLOT = OFF_BAR + 8 * B_COUNT;
-constexpr int OFF_UNITS = (OFF_TSLOT + 16 + 15) / 16 * 16;  // self-planned unit table
-constexpr int kSmem = OFF_UNITS + (int)sizeof(UnitInfo) * (kSelfPlanMaxReqs + 1) + 1024;
-static_assert(kSmem <= 227 * 1024, "one CTA per SM");
+// E4M3 cache. A K or V tile: [128 keys][128 B] (one 2 KB copy per block);
+// the q' operand: [2 slots][hi, lo][8 rows][128 B], then 1/2^e as [2 slots][8]
+// floats; P'^T: [32 rows][128 B]. N = 32: slot s is rows / columns 16 s ..,
+// the hi terms first.
+template <>
+struct TcL<true> {
+  static constexpr int kStages = 5;
+  static constexpr int kGroup = 1024;
+  static constexpr int kHalfOff = 0;
+  static constexpr int kKvTile = 16384;
+  static constexpr int kQBytes = 4096 + 1024;
+  static constexpr int kN = 32;
+  static constexpr int kSlotCols = 16;
+  static constexpr int kKStep = 32;
+  static constexpr int kPBytes = 4096;
+  static constexpr uint32_t kTmemCols = 128;
+};
+
+// S^T in TMEM and P^T in shared memory are kept in this many buffers: a
+// tile's S can be computed while the softmax of the tile before runs (three
+// buffers measured no faster).
+constexpr int kSP = 2;
+
+template <bool F8>
+struct TcSmem {
+  using L = TcL<F8>;
+  static constexpr int kStageBytes = 2 * L::kKvTile + L::kQBytes;
+  static constexpr int OFF_STAGE = 0;
+  static constexpr int OFF_P = L::kStages * kStageBytes;    // kSP buffers of P^T
+  static constexpr int OFF_REC = OFF_P + kSP * L::kPBytes;  // one tile record per stage
+  static constexpr int OFF_XCH = OFF_REC + L::kStages * 64;  // [2][4 warps][16] floats
+  static constexpr int OFF_BAR = OFF_XCH + 2 * 4 * 16 * 4;
+  // barriers: FULL[stages], EMPTY[stages], S[kSP], P_READY[kSP], P_FREE[kSP], XCH[2], DRAIN
+  static constexpr int B_FULL = 0, B_EMPTY = L::kStages, B_S = 2 * L::kStages,
+                       B_PREADY = B_S + kSP, B_PFREE = B_S + 2 * kSP, B_XCH = B_S + 3 * kSP,
+                       B_DRAIN = B_XCH + 2, B_COUNT = B_DRAIN + 1;
+  static constexpr int OFF_TSLOT = OFF_BAR + 8 * B_COUNT;
+  static constexpr int OFF_UNITS = (OFF_TSLOT + 16 + 15) / 16 * 16;  // self-planned unit table
+  static constexpr int SMEM = OFF_UNITS + (int)sizeof(UnitInfo) * (kSelfPlanMaxReqs + 1) + 1024;
+  static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+  static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte alignment of swizzled tiles");
+  // TMEM columns: S^T buffers at 0, kN, 2 kN, O^T after them
+  static constexpr uint32_t kTmS = 0, kTmO = kSP * L::kN;
+  static_assert(kTmO + L::kN <= L::kTmemCols, "S^T buffers and O^T fit the allocation");
+};
 
 // A tile covers the end of one portion (a (token, kv head) part of this
 // CTA's slice) and possibly the start of the next. Portion n of the CTA takes
@@ -130,11 +189,33 @@ struct Rec {
 };
 static_assert(sizeof(Rec) == 64, "records are 64 bytes");
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D; a_mn / b_mn
-// select the M/N-major (transposed) form of each operand.
-constexpr uint32_t idesc_tc(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+// Instruction descriptor with fp32 D: kind::f16 with bf16 A/B, or (f8)
+// kind::f8f6f4 with E4M3 A/B (format code 0); a_mn / b_mn select the
+// M/N-major (transposed) form of each operand.
+constexpr uint32_t idesc_tc(int M, int N, bool a_mn, bool b_mn, bool f8 = false) {
+  return (1u << 4) | (f8 ? 0u : ((1u << 7) | (1u << 10))) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], E4M3 inputs, fp32 accumulate.
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
 }
 
 // TMEM loads/stores of N consecutive 32-bit columns of the warp's 32 lanes.
@@ -221,15 +302,22 @@ __device__ __forceinline__ float warp_reduce_heads(float (&v)[G], int lane) {
 }  // namespace
 
 struct TcDecodeParams {
-  CUtensorMap tm_q;  // q as {64, T * Hq rows, 2 halves}, box {64, 8, 2}, 128B swizzle
-  CUtensorMap tm_k;  // k_cache as {64, 8, 2, blocks * Hkv * 2 groups}, box {64, 8, 2, 2}
+  // bf16: q as {64, T * Hq rows, 2 halves}, box {64, 8, 2}; a cache as
+  // {64, 8, 2, blocks * Hkv * 2 groups}, box {64, 8, 2, 2}.
+  // E4M3: the split q' rows as {128 B, T * Hq rows, 2 (hi, lo)}, box
+  // {128, 8, 2}; a cache as {128 B, blocks * Hkv * 16 rows}, box {128, 16}.
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
   CUtensorMap tm_v;
   DecodeParams d;
 };
 
-template <int G>
+template <int G, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_decode_tc_kernel(const __grid_constant__ TcDecodeParams tp) {
+  using L = TcL<F8>;
+  using M = TcSmem<F8>;
+  constexpr int kStages = L::kStages;
   const DecodeParams& p = tp.d;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -239,35 +327,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The merge pass may be placed as CTAs of this grid retire (it waits for
   // the whole grid before reading).
   griddep_launch_dependents();
-  auto BAR = [&](int i) -> uint32_t { return base + OFF_BAR + 8u * (uint32_t)i; };
+  auto BAR = [&](int i) -> uint32_t { return base + M::OFF_BAR + 8u * (uint32_t)i; };
   auto wait = [&](int i, int parity) -> bool {
     if (mbar_wait_bounded(BAR(i), (uint32_t)parity & 1u)) return true;
     report_error(p.err, PA_DEVERR_WAIT_TIMEOUT, 2000 + i);
     return false;
   };
-  Rec* const recs = reinterpret_cast<Rec*>(gb + OFF_REC);
+  Rec* const recs = reinterpret_cast<Rec*>(gb + M::OFF_REC);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B_COUNT; ++i) {
+    for (int i = 0; i < M::B_COUNT; ++i) {
       // P_READY and the exchanges are arrived at by the 128 softmax threads;
       // every other barrier once (an expect_tx arrive or an MMA commit).
-      const bool by_softmax = i == B_PREADY || i == B_PREADY + 1 || i == B_XCH || i == B_XCH + 1;
+      const bool by_softmax = (i >= M::B_PREADY && i < M::B_PREADY + kSP) || i == M::B_XCH ||
+                              i == M::B_XCH + 1;
       mbar_init(BAR(i), by_softmax ? 128 : 1);
     }
     fence_barrier_init();
   }
-  // Rows past the group in each slot of the q and P^T operands stay zero for
-  // good (TMA and the softmax write only the first G rows of a slot), and so
-  // do the padded MMA columns.
+  // The query operands of every stage and the P^T buffers start at zero:
+  // rows past the group stay zero (bf16) or hold other heads' rows (TMA
+  // copies 8 rows per slot), which only reach the slot's unused columns.
   for (int st = 0; st < kStages; ++st)
-    for (int idx = threadIdx.x; idx < kQBytes / 16; idx += kThreads)
-      reinterpret_cast<uint4*>(gb + OFF_STAGE + st * kStageBytes + 2 * kKvTile)[idx] =
+    for (int idx = threadIdx.x; idx < L::kQBytes / 16; idx += kThreads)
+      reinterpret_cast<uint4*>(gb + M::OFF_STAGE + st * M::kStageBytes + 2 * L::kKvTile)[idx] =
           make_uint4(0u, 0u, 0u, 0u);
-  for (int idx = threadIdx.x; idx < (2 * kNbuf) / 16; idx += kThreads)
-    reinterpret_cast<uint4*>(gb + OFF_P)[idx] = make_uint4(0u, 0u, 0u, 0u);
+  for (int idx = threadIdx.x; idx < (kSP * L::kPBytes) / 16; idx += kThreads)
+    reinterpret_cast<uint4*>(gb + M::OFF_P)[idx] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
   if (warp == 5) {
-    tmem_alloc(base + OFF_TSLOT, kTmemCols);
+    tmem_alloc(base + M::OFF_TSLOT, L::kTmemCols);
     tmem_relinquish();
   }
 
@@ -278,26 +367,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   int W, K;
   bool waited = false;  // griddepcontrol.wait done (the plan and the KV write are visible)
   if (p.self_plan) {
-    UnitInfo* const su = reinterpret_cast<UnitInfo*>(gb + OFF_UNITS);
+    UnitInfo* const su = reinterpret_cast<UnitInfo*>(gb + M::OFF_UNITS);
     __shared__ int s_tot[kWarps];
     const int R = p.num_reqs, T = p.num_tokens, Hkv_ = p.num_kv_heads;
     int carry = 0;
     for (int r0 = 0; r0 < R; r0 += kThreads) {
       const int r = r0 + (int)threadIdx.x;
-      int n = 0, q0 = T, L = 0;
+      int n = 0, q0 = T, Lr = 0;
       if (r < R) {
         q0 = __ldg(p.qsl + r);
         const int q1 = __ldg(p.qsl + r + 1);
-        L = __ldg(p.seq_lens + r);
+        Lr = __ldg(p.seq_lens + r);
         const int qlen = q1 - q0;
         if (q0 < 0 || q1 < q0 || q1 > T) {
           report_error(p.err, PA_DEVERR_QSL, r);
           q0 = T;
-        } else if (L < qlen || qlen > 1 || (L + kBlockSize - 1) / kBlockSize > p.max_blocks_per_req ||
-                   qlen > p.max_query_len || L > p.max_seq_len) {
+        } else if (Lr < qlen || qlen > 1 || (Lr + kBlockSize - 1) / kBlockSize > p.max_blocks_per_req ||
+                   qlen > p.max_query_len || Lr > p.max_seq_len) {
           report_error(p.err, PA_DEVERR_LENGTHS, r);
         } else if (qlen == 1) {
-          n = Hkv_ * ((L + kBlockSize - 1) / kBlockSize);
+          n = Hkv_ * ((Lr + kBlockSize - 1) / kBlockSize);
         }
       }
       int incl = n;  // warp inclusive scan of positions
@@ -310,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       int off = carry;
       for (int w2 = 0; w2 < warp; ++w2) off += s_tot[w2];
-      if (r < R) su[r] = UnitInfo{q0, r, n > 0 ? L : 0, off + incl - n};
+      if (r < R) su[r] = UnitInfo{q0, r, n > 0 ? Lr : 0, off + incl - n};
       for (int w2 = 0; w2 < kWarps; ++w2) carry += s_tot[w2];
       __syncthreads();
     }
@@ -331,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + OFF_TSLOT);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + M::OFF_TSLOT);
 
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
   const int w = (int)blockIdx.x;
@@ -388,10 +477,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.merge_tasks[w] = task;
       }
     }
+    if constexpr (F8) {
+      // the split query rows come from the preceding grid (launch_qsplit)
+      if (!waited) {
+        griddep_wait();
+        waited = true;
+      }
+    }
 
     struct Meta {
       SlotRec s[2];
-      int nblk;  // blocks in the tile; 0: no more tiles
+      int nblk;      // blocks in the tile; 0: no more tiles
       int last_blk;  // the tile holds a portion's last block (a decode's newest token)
       int pid, kvl;  // this lane's block id (loaded now, used two tiles later) and kv head
     };
@@ -455,11 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue = [&](const Meta& cur, Meta& nxt2) -> bool {  // false: stop
       nxt2 = next_tile();
       const int st = i % kStages;
-      if (i >= kStages && !wait(B_EMPTY + st, (i / kStages) - 1)) {
+      if (i >= kStages && !wait(M::B_EMPTY + st, (i / kStages) - 1)) {
         ok = false;
         return false;
       }
-      const uint32_t full = BAR(B_FULL + st);
+      const uint32_t full = BAR(M::B_FULL + st);
       if (cur.nblk == 0) {
         if (lane == 0) {
           recs[st].s[0] = SlotRec{0, 0, 0, 0, 0, 0, 0, 1};
@@ -473,7 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         recs[st].s[0] = cur.s[0];
         recs[st].s[1] = cur.s[1];
-        mbar_arrive_expect_tx(full, (uint32_t)cur.nblk * 2u * 4096u + (uint32_t)nq * 2048u);
+        // per block: K and V (4 KB each bf16, 2 KB each E4M3); per active
+        // slot: its 8 query-operand rows (2 KB), and E4M3's 32 B of scales
+        mbar_arrive_expect_tx(full, (uint32_t)cur.nblk * (F8 ? 4096u : 8192u) +
+                                        (uint32_t)nq * (F8 ? 2048u + 32u : 2048u));
       }
       __syncwarp();
       // a decode's newest token, written by the preceding grid, sits in its
@@ -482,26 +581,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         griddep_wait();
         waited = true;
       }
-      const uint32_t sbase = base + OFF_STAGE + st * kStageBytes;
+      const uint32_t sbase = base + M::OFF_STAGE + st * M::kStageBytes;
       if (lane < cur.nblk) {
         int pid = cur.pid;
         if (pid < 0 || pid >= p.num_blocks) {
           report_error(p.err, PA_DEVERR_BLOCK_ID, lane);
           pid = 0;
         }
-        const int grp = (pid * Hkv + cur.kvl) * (kBlockSize / 8);  // the block's first 8-key group
-        const uint32_t dst = sbase + lane * 2 * kGroup;
-        tma_load_4d(dst, &tp.tm_k, 0, 0, 0, grp, full);
-        tma_load_4d(dst + kKvTile, &tp.tm_v, 0, 0, 0, grp, full);
+        if constexpr (F8) {
+          const int row = (pid * Hkv + cur.kvl) * kBlockSize;  // the block's first row
+          tma_load_2d(sbase + lane * 2048, &tp.tm_k, 0, row, full);
+          tma_load_2d(sbase + L::kKvTile + lane * 2048, &tp.tm_v, 0, row, full);
+        } else {
+          const int grp = (pid * Hkv + cur.kvl) * (kBlockSize / 8);  // the block's first 8-key group
+          tma_load_4d(sbase + lane * 2 * L::kGroup, &tp.tm_k, 0, 0, 0, grp, full);
+          tma_load_4d(sbase + L::kKvTile + lane * 2 * L::kGroup, &tp.tm_v, 0, 0, 0, grp, full);
+        }
       }
       const int qflags = lane == 0 ? cur.s[0].flags : cur.s[1].flags;
-      if (lane < 2 && (qflags & F_ACTIVE)) {  // q rows of slot `lane`
-        const int qrow = lane == 0 ? cur.s[0].tok * Hq + cur.s[0].kv * G
-                                   : cur.s[1].tok * Hq + cur.s[1].kv * G;
-        // 8 q rows from the group's first (rows past the group are other
+      if (lane < 2 && (qflags & F_ACTIVE)) {  // the query operand rows of slot `lane`
+        const int qtok = lane == 0 ? cur.s[0].tok : cur.s[1].tok;
+        const int qkv = lane == 0 ? cur.s[0].kv : cur.s[1].kv;
+        // 8 rows from the group's first (rows past the group are other
         // heads' queries, or zeros past the end: they only feed the slot's
         // unused columns)
-        tma_load_3d(sbase + 2 * kKvTile + lane * kGroup, &tp.tm_q, 0, qrow, 0, full);
+        tma_load_3d(sbase + 2 * L::kKvTile + lane * 2048, &tp.tm_q, 0, qtok * Hq + qkv * G, 0,
+                    full);
+        if constexpr (F8)  // the group's 8 inverse scales
+          bulk_load(sbase + 2 * L::kKvTile + 4096 + lane * 32,
+                    p.qinv + ((size_t)qtok * Hkv + qkv) * 8, 32, full);
       }
       ++i;
       return true;
@@ -514,92 +622,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // every copy issued has landed before the CTA may exit
     for (int j = i > kStages ? i - kStages : 0; j < i; ++j)
-      mbar_wait_bounded(BAR(B_FULL + j % kStages), (uint32_t)(j / kStages) & 1u);
+      mbar_wait_bounded(BAR(M::B_FULL + j % kStages), (uint32_t)(j / kStages) & 1u);
   } else if (warp == 5) {
     // ======================= MMA issuer (lane 0) =======================
     // Two kinds of work, each in tile order: S(j) once tile j has landed and
-    // S buffer j % 2 is free (the P.V of tile j - 2 issued, hence its softmax
-    // done), and O(j) = P.V once the softmax of tile j is done. Whichever is
+    // S buffer j % kSP is free (the P.V of tile j - kSP issued, hence its
+    // softmax done), and O(j) = P.V once the softmax of tile j is done. Whichever is
     // ready is issued, the P.V first: it frees a stage for the producer. O^T
     // always accumulates: its columns start at zero and an epilogue zeroes a
     // slot's columns after reading them.
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_tc(128, 16, false, false);
-      constexpr uint32_t id_o = idesc_tc(128, 16, true, false);
-      const uint64_t kdesc = smem_desc_sw128(base, 16, kGroup);         // K-major: K tile, q rows
-      const uint64_t pdesc = smem_desc_sw128(base, 16, 1024);           // K-major: P^T
-      const uint64_t vdesc = smem_desc_sw128(base, kHalfOff, kGroup);   // M/N-major: V^T
+      constexpr uint32_t id_s = idesc_tc(128, L::kN, false, false, F8);
+      constexpr uint32_t id_o = idesc_tc(128, L::kN, true, false, F8);
+      // K-major: the K tile and the query operand (8-row groups kGroup apart
+      // in the K tile, 2 KB / 1 KB apart in the query operand)
+      const uint64_t kdesc = smem_desc_sw128(base, 16, L::kGroup);
+      const uint64_t qdesc = smem_desc_sw128(base, 16, F8 ? 1024 : 2048);
+      const uint64_t pdesc = smem_desc_sw128(base, 16, 1024);  // K-major: P^T
+      // M/N-major: V^T (8-key groups kGroup apart; bf16: the 64-dim halves kHalfOff apart)
+      const uint64_t vdesc = smem_desc_sw128(base, F8 ? 16 : L::kHalfOff, L::kGroup);
+      constexpr int kSteps = 128 / L::kKStep;  // MMAs per product (K = 128 dims or keys)
       int ns = 0, no = 0;  // next tile for S, next tile for P.V
       bool end_seen = false;
       uint32_t spins = 0;
       uint64_t t0 = 0;
 #pragma unroll 1
       while (!(end_seen && no == ns)) {
-        if (no < ns && mbar_test(BAR(B_PREADY + (no & 1)), (uint32_t)(no >> 1) & 1u)) {
+        if (no < ns && mbar_test(BAR(M::B_PREADY + no % kSP), (uint32_t)(no / kSP) & 1u)) {
           tc_fence_after();
           const int st = no % kStages;
-          const uint64_t a0 = vdesc + ((uint64_t)(OFF_STAGE + st * kStageBytes + kKvTile) >> 4);
-          const uint64_t b0 = pdesc + ((uint64_t)(OFF_P + (no & 1) * kNbuf) >> 4);
+          const uint64_t a0 = vdesc + ((uint64_t)(M::OFF_STAGE + st * M::kStageBytes + L::kKvTile) >> 4);
+          const uint64_t b0 = pdesc + ((uint64_t)(M::OFF_P + (no % kSP) * L::kPBytes) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // keys 16 ks .. 16 ks + 15: groups 2 ks, 2 ks + 1
-            umma_bf16(tmem + kTmO, a0 + (uint64_t)((ks * 2 * kGroup) >> 4),
-                      b0 + (uint64_t)(((ks >> 2) * kNhalf + (ks & 3) * 32) >> 4), id_o, 1u);
-          umma_commit(BAR(B_EMPTY + st));
-          umma_commit(BAR(B_PFREE + (no & 1)));
+          for (int ks = 0; ks < kSteps; ++ks) {
+            if constexpr (F8) {  // keys 32 ks .. 32 ks + 31: 4 rows of 8-key groups
+              umma_e4m3(tmem + M::kTmO, a0 + (uint64_t)((ks * 4 * L::kGroup) >> 4),
+                        b0 + (uint64_t)((ks * 32) >> 4), id_o, 1u);
+            } else {  // keys 16 ks .. 16 ks + 15: groups 2 ks, 2 ks + 1
+              umma_bf16(tmem + M::kTmO, a0 + (uint64_t)((ks * 2 * L::kGroup) >> 4),
+                        b0 + (uint64_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4), id_o, 1u);
+            }
+          }
+          umma_commit(BAR(M::B_EMPTY + st));
+          umma_commit(BAR(M::B_PFREE + no % kSP));
           ++no;
           spins = 0;
-        } else if (!end_seen && ns <= no + 1 &&
-                   mbar_test(BAR(B_FULL + ns % kStages), (uint32_t)(ns / kStages) & 1u)) {
+        } else if (!end_seen && ns <= no + kSP - 1 &&
+                   mbar_test(BAR(M::B_FULL + ns % kStages), (uint32_t)(ns / kStages) & 1u)) {
           const int st = ns % kStages;
           if (recs[st].s[0].pad) {
             end_seen = true;
           } else {
             tc_fence_after();
-            const uint64_t a0 = kdesc + ((uint64_t)(OFF_STAGE + st * kStageBytes) >> 4);
-            const uint64_t b0 = kdesc + ((uint64_t)(OFF_STAGE + st * kStageBytes + 2 * kKvTile) >> 4);
+            const uint64_t a0 = kdesc + ((uint64_t)(M::OFF_STAGE + st * M::kStageBytes) >> 4);
+            const uint64_t b0 =
+                qdesc + ((uint64_t)(M::OFF_STAGE + st * M::kStageBytes + 2 * L::kKvTile) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks)  // head dims 16 ks .. 16 ks + 15
-              umma_bf16(tmem + kTmS + 16 * (ns & 1),
-                        a0 + (uint64_t)(((ks >> 2) * kHalfOff + (ks & 3) * 32) >> 4),
-                        b0 + (uint64_t)(((ks >> 2) * kHalfOff + (ks & 3) * 32) >> 4), id_s,
-                        ks > 0 ? 1u : 0u);
-            umma_commit(BAR(B_S + (ns & 1)));
+            for (int ks = 0; ks < kSteps; ++ks) {  // head dims ks * kKStep ..
+              if constexpr (F8) {
+                umma_e4m3(tmem + M::kTmS + L::kN * (ns % kSP), a0 + (uint64_t)((ks * 32) >> 4),
+                          b0 + (uint64_t)((ks * 32) >> 4), id_s, ks > 0 ? 1u : 0u);
+              } else {
+                umma_bf16(tmem + M::kTmS + L::kN * (ns % kSP),
+                          a0 + (uint64_t)(((ks >> 2) * L::kHalfOff + (ks & 3) * 32) >> 4),
+                          b0 + (uint64_t)(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4), id_s,
+                          ks > 0 ? 1u : 0u);
+              }
+            }
+            umma_commit(BAR(M::B_S + ns % kSP));
             ++ns;
           }
           spins = 0;
         } else if (++spins > 64) {  // nothing ready: give up after ~2 s without progress
           if (spins == 65) t0 = global_timer_ns();
           if (global_timer_ns() - t0 > 2000000000ull) {
-            report_error(p.err, PA_DEVERR_WAIT_TIMEOUT, 2000 + B_PREADY);
+            report_error(p.err, PA_DEVERR_WAIT_TIMEOUT, 2000 + M::B_PREADY);
             break;
           }
         }
       }
       // every MMA issued above has completed before TMEM is released
-      umma_commit(BAR(B_DRAIN));
-      mbar_wait_bounded(BAR(B_DRAIN), 0);
+      umma_commit(BAR(M::B_DRAIN));
+      mbar_wait_bounded(BAR(M::B_DRAIN), 0);
     }
     __syncwarp();
   } else {
     // ======================= softmax + epilogue (warps 0-3) =======================
     const int m = warp * 32 + lane;  // key row of S^T and head dim of O^T: the TMEM lane
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    float* const xch = reinterpret_cast<float*>(gb + OFF_XCH);
+    float* const xch = reinterpret_cast<float*>(gb + M::OFF_XCH);
     int nx = 0;  // exchanges done
-    // Per-(slot, head) max or sum over the 128 softmax threads: warp
-    // reduction, then the four warps meet on an mbarrier (bounded wait).
-    // Exchange k uses buffer and barrier k % 2: a buffer is rewritten only
-    // after every thread has passed the other barrier, i.e. has read this one.
-    auto block_reduce = [&](auto& v, auto tag_n, bool is_max) -> bool {
-      constexpr int N = decltype(tag_n)::value;
-      const float x = is_max ? warp_reduce_heads<N, true>(v, lane) : warp_reduce_heads<N, false>(v, lane);
+    // Per-head max or sum over the 128 softmax threads: warp reduction, then
+    // the four warps meet on an mbarrier (bounded wait). Exchange k uses
+    // buffer and barrier k % 2: a buffer is rewritten only after every thread
+    // has passed the other barrier, i.e. has read this one.
+    auto block_reduce = [&](float (&v)[G], bool is_max) -> bool {
+      const float x = is_max ? warp_reduce_heads<G, true>(v, lane) : warp_reduce_heads<G, false>(v, lane);
       const int kx = nx++;
       float* const xb = xch + (kx & 1) * 64;
-      if (lane < N) xb[warp * 16 + tc_head_of_lane<N>(lane)] = x;
-      mbar_arrive(BAR(B_XCH + (kx & 1)));
-      if (!wait(B_XCH + (kx & 1), kx >> 1)) return false;
+      if (lane < G) xb[warp * 16 + tc_head_of_lane<G>(lane)] = x;
+      mbar_arrive(BAR(M::B_XCH + (kx & 1)));
+      if (!wait(M::B_XCH + (kx & 1), kx >> 1)) return false;
 #pragma unroll
-      for (int h = 0; h < N; ++h) {
+      for (int h = 0; h < G; ++h) {
         const float a = xb[h], b = xb[16 + h], c = xb[32 + h], d = xb[48 + h];
         v[h] = is_max ? fmaxf(fmaxf(a, b), fmaxf(c, d)) : (a + b) + (c + d);
       }
@@ -607,11 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // O^T starts at zero (the P.V MMAs always accumulate)
     {
-      uint32_t z[16];
+      uint32_t z[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) z[c] = 0u;
-      tm_st<8>(trow + kTmO, *reinterpret_cast<uint32_t(*)[8]>(z));
-      tm_st<8>(trow + kTmO + 8, *reinterpret_cast<uint32_t(*)[8]>(z + 8));
+      for (int c = 0; c < 8; ++c) z[c] = 0u;
+#pragma unroll
+      for (int c = 0; c < L::kN; c += 8) tm_st<8>(trow + M::kTmO + c, z);
       tmem_wait_st();
     }
     float mref[2][G], lth[2][G];
@@ -624,31 +749,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     // P^T rows of slot j in buffer b may be non-zero: bit 2b + j (uniform)
     int dirty = 0;
-    // P^T[8 slot + h][m] of buffer b: row 8 slot + h, 16-byte unit (m % 64) / 8
-    // swizzled by h, half m / 64
+    // bf16: P^T[8 slot + h][m] of buffer b: half m / 64, row 8 slot + h,
+    // 16-byte unit (m % 64) / 8 swizzled by h
     auto prow = [&](int b, int j, int h) -> uint16_t* {
-      return reinterpret_cast<uint16_t*>(gb + OFF_P + b * kNbuf + (m >> 6) * kNhalf + j * 1024 +
-                                         h * 128 + ((((m & 63) >> 3) ^ h) << 4) + (m & 7) * 2);
+      return reinterpret_cast<uint16_t*>(gb + M::OFF_P + b * L::kPBytes + (m >> 6) * 2048 +
+                                         j * 1024 + h * 128 + ((((m & 63) >> 3) ^ h) << 4) +
+                                         (m & 7) * 2);
     };
+    // E4M3: P'^T row r = 16 slot + 8 hl + h of buffer b, byte m: 16-byte unit
+    // m / 16 swizzled by h
+    auto prow8 = [&](int b, int r) -> unsigned char* {
+      return gb + M::OFF_P + b * L::kPBytes + r * 128 + ((((m >> 4) ^ (r & 7))) << 4) + (m & 15);
+    };
+    // The reference max moves only when a tile's max exceeds it by more than
+    // this (log2 units): 2^8 for bf16 P, 0.75 for E4M3 P' = 256 p <= 430.
+    constexpr float kSlack = F8 ? 0.75f : 8.f;
     int i = 0;
     bool ok = true;
 #pragma unroll 1
     while (ok) {
       const int st = i % kStages;
-      if (!wait(B_FULL + st, i / kStages)) { ok = false; break; }  // the tile record is visible
+      if (!wait(M::B_FULL + st, i / kStages)) { ok = false; break; }  // the tile record is visible
       const SlotRec r0 = recs[st].s[0], r1 = recs[st].s[1];
       if (r0.pad) break;
-      if (!wait(B_S + (i & 1), i >> 1)) { ok = false; break; }
+      const int b = i % kSP;  // S^T and P^T buffer of this tile
+      if (!wait(M::B_S + b, i / kSP)) { ok = false; break; }
       tc_fence_after();
-      const int b = i & 1;
       // this thread's key: slot my (-1: no key), valid when inside its sequence
       const bool in0 = (r0.flags & F_ACTIVE) && m >= r0.row0 && m < r0.row0 + r0.nrows;
       const bool in1 = (r1.flags & F_ACTIVE) && m >= r1.row0 && m < r1.row0 + r1.nrows;
       const int my = in0 ? 0 : (in1 ? 1 : -1);
       const bool valid = in0 ? (r0.key0 + (m - r0.row0) < r0.len)
                              : (in1 ? (r1.key0 + (m - r1.row0) < r1.len) : false);
-      // P^T buffer b is free once the P.V of tile i - 2 has completed
-      if (i >= 2 && !wait(B_PFREE + b, (i - 2) >> 1)) { ok = false; break; }
+      // P^T buffer b is free once the P.V of tile i - kSP has completed
+      if (i >= kSP && !wait(M::B_PFREE + b, i / kSP - 1)) { ok = false; break; }
       // One pass per active slot (two only where the tile crosses from one
       // portion into the next): the slot's scores, its maxima, P^T rows.
       const int nact = ((r0.flags & F_ACTIVE) ? 1 : 0) + ((r1.flags & F_ACTIVE) ? 1 : 0);
@@ -657,21 +791,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jj = (pass == 0 && (r0.flags & F_ACTIVE)) ? 0 : 1;
         const int fl = jj ? r1.flags : r0.flags;
         const bool mine = valid && my == jj;  // this thread's key belongs to slot jj
-        uint32_t sr[G];
-        tm_ld<G>(trow + kTmS + 16 * b + 8 * jj, sr);
-        tmem_wait_ld();
-        float t[G], tm[G], mr[G], lt[G];
+        const uint32_t scol = M::kTmS + L::kN * b + L::kSlotCols * jj;
+        float t[G];
+        if constexpr (F8) {  // hi and lo column groups, the row scales undone
+          uint32_t shi[G], slo[G];
+          tm_ld<G>(trow + scol, shi);
+          tm_ld<G>(trow + scol + 8, slo);
+          tmem_wait_ld();
+          const float* const inv = reinterpret_cast<const float*>(
+              gb + M::OFF_STAGE + st * M::kStageBytes + 2 * L::kKvTile + 4096 + jj * 32);
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            t[h] = mine ? (__uint_as_float(shi[h]) + __uint_as_float(slo[h])) * (inv[h] * p.scale_log2)
+                        : -INFINITY;
+        } else {
+          uint32_t sr[G];
+          tm_ld<G>(trow + scol, sr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < G; ++h) t[h] = mine ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+        }
+        float tm[G], mr[G], lt[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          t[h] = mine ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
           tm[h] = t[h];
           mr[h] = jj ? mref[1][h] : mref[0][h];
           lt[h] = jj ? lth[1][h] : lth[0][h];
         }
-        if (!block_reduce(tm, std::integral_constant<int, G>{}, true)) { ok = false; break; }
+        if (!block_reduce(tm, true)) { ok = false; break; }
         // reference maxima: a portion's first tile sets them (it holds the
         // portion's first key, so they are finite); later tiles move them
-        // only by more than 2^8, rescaling the slot's O^T columns
+        // only by more than kSlack, rescaling the slot's O^T columns
         bool resc = false;
         float alpha[G];
 #pragma unroll
@@ -680,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (fl & F_FIRST) {
             mr[h] = tm[h];
             lt[h] = 0.f;
-          } else if (tm[h] > mr[h] + 8.f) {
+          } else if (tm[h] > mr[h] + kSlack) {
             alpha[h] = exp2f(mr[h] - tm[h]);
             mr[h] = tm[h];
             resc = true;
@@ -688,18 +838,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (resc) {  // uniform: every thread holds the same maxima
           // O^T is stable once the previous tile's P.V has completed
-          if (!wait(B_PFREE + ((i - 1) & 1), (i - 1) >> 1)) { ok = false; break; }
+          if (!wait(M::B_PFREE + (i - 1) % kSP, (i - 1) / kSP)) { ok = false; break; }
           tc_fence_after();
-          uint32_t o[G];
-          tm_ld<G>(trow + kTmO + 8 * jj, o);
-          tmem_wait_ld();
+          const uint32_t ocol = M::kTmO + L::kSlotCols * jj;
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-            lt[h] *= alpha[h];
+          for (int g = 0; g < L::kSlotCols; g += 8) {  // E4M3: the hi and the lo group
+            uint32_t o[G];
+            tm_ld<G>(trow + ocol + g, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < G; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+            tm_st<G>(trow + ocol + g, o);
           }
-          tm_st<G>(trow + kTmO + 8 * jj, o);
           tmem_wait_st();
+#pragma unroll
+          for (int h = 0; h < G; ++h) lt[h] *= alpha[h];
         }
         float pr[G];
 #pragma unroll
@@ -717,12 +870,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             lth[0][h] = lt[h];
           }
         }
+        if constexpr (F8) {
+          // P' = 256 p as E4M3 hi + lo, one byte per row of the slot
 #pragma unroll
-        for (int h = 0; h < G; ++h) *prow(b, jj, h) = bf16_bits(pr[h]);
+          for (int h = 0; h < G; h += 2) {
+            const float x0 = 256.f * pr[h], x1 = h + 1 < G ? 256.f * pr[h + 1] : 0.f;
+            const uint16_t hi = float2_to_e4m3x2(x0, x1);
+            const float2 hf = e4m3x2_to_float2(hi);
+            const uint16_t lo = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
+            *prow8(b, 16 * jj + h) = (unsigned char)(hi & 0xffu);
+            *prow8(b, 16 * jj + 8 + h) = (unsigned char)(lo & 0xffu);
+            if (h + 1 < G) {
+              *prow8(b, 16 * jj + h + 1) = (unsigned char)(hi >> 8);
+              *prow8(b, 16 * jj + 8 + h + 1) = (unsigned char)(lo >> 8);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < G; ++h) *prow(b, jj, h) = bf16_bits(pr[h]);
+        }
         dirty |= 1 << (2 * b + jj);
         if (nact == 1 && (dirty & (1 << (2 * b + (1 - jj))))) {  // the idle slot's rows to zero
+          if constexpr (F8) {
 #pragma unroll
-          for (int h = 0; h < G; ++h) *prow(b, 1 - jj, h) = 0;
+            for (int h = 0; h < G; ++h) {
+              *prow8(b, 16 * (1 - jj) + h) = 0;
+              *prow8(b, 16 * (1 - jj) + 8 + h) = 0;
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < G; ++h) *prow(b, 1 - jj, h) = 0;
+          }
           dirty &= ~(1 << (2 * b + (1 - jj)));
         }
       }
@@ -731,22 +909,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // A key past the sequence end (or a block slot this tile did not
         // load) has P = 0, but its V row may hold anything, NaN included, and
         // 0 * NaN would poison O: clear the row.
-        unsigned char* const vrow =
-            gb + OFF_STAGE + st * kStageBytes + kKvTile + (m >> 3) * kGroup + (m & 7) * 128;
+        if constexpr (F8) {
+          unsigned char* const vrow = gb + M::OFF_STAGE + st * M::kStageBytes + L::kKvTile + m * 128;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+          for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(vrow + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          unsigned char* const vrow = gb + M::OFF_STAGE + st * M::kStageBytes + L::kKvTile +
+                                      (m >> 3) * L::kGroup + (m & 7) * 128;
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4*>(vrow + c * kHalfOff + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vrow + c * L::kHalfOff + q * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
       fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
       tc_fence_before();
-      mbar_arrive(BAR(B_PREADY + (i & 1)));
+      mbar_arrive(BAR(M::B_PREADY + b));
 
       if ((r0.flags | r1.flags) & F_LAST) {
         // ---- epilogue of the portions ending here: O^T complete once tile
         // i's P.V is ----
-        if (!wait(B_PFREE + (i & 1), i >> 1)) { ok = false; break; }
+        if (!wait(M::B_PFREE + b, i / kSP)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -755,15 +939,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           float ls[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) ls[h] = lth[j][h];
-          if (!block_reduce(ls, std::integral_constant<int, G>{}, false)) { ok = false; break; }
-          uint32_t o[8];
-          tm_ld<8>(trow + kTmO + 8 * j, o);
-          tmem_wait_ld();
+          if (!block_reduce(ls, false)) { ok = false; break; }
+          const uint32_t ocol = M::kTmO + L::kSlotCols * j;
+          float o[G];
+          {
+            uint32_t oa[G];
+            tm_ld<G>(trow + ocol, oa);
+            if constexpr (F8) {  // hi + lo groups, back from P' = 256 p
+              uint32_t ob[G];
+              tm_ld<G>(trow + ocol + 8, ob);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < G; ++h)
+                o[h] = (__uint_as_float(oa[h]) + __uint_as_float(ob[h])) * (1.f / 256.f);
+            } else {
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < G; ++h) o[h] = __uint_as_float(oa[h]);
+            }
+          }
           if (rc.flags & F_WHOLE) {
             uint16_t* const orow = p.out + ((size_t)rc.tok * Hq + (size_t)rc.kv * G) * kD + m;
 #pragma unroll
-            for (int h = 0; h < G; ++h)
-              orow[h * kD] = bf16_bits(__uint_as_float(o[h]) * (p.v_scale / ls[h]));
+            for (int h = 0; h < G; ++h) orow[h * kD] = bf16_bits(o[h] * (p.v_scale / ls[h]));
           } else {
             // a partial (m, l, o) for the merge pass in slot u + w: tokens
             // increase with the position order, so the slot is unique per portion
@@ -777,13 +975,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
 #pragma unroll
-            for (int h = 0; h < G; ++h) __stcg(slot + 16 + h * kD + m, __uint_as_float(o[h]));
+            for (int h = 0; h < G; ++h) __stcg(slot + 16 + h * kD + m, o[h]);
           }
           // the slot's columns start the next portion at zero
           uint32_t z[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) z[c] = 0u;
-          tm_st<8>(trow + kTmO + 8 * j, z);
+#pragma unroll
+          for (int g = 0; g < L::kSlotCols; g += 8) tm_st<8>(trow + ocol + g, z);
           tmem_wait_st();
         }
         if (!ok) break;
@@ -797,8 +996,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, L::kTmemCols);
   }
+}
+
+// One warp per (token, kv head): each of the G query rows is scaled by the
+// power of two 2^e that brings its largest magnitude into [128, 256) and
+// split into E4M3 terms hi = E4M3(x 2^e), lo = E4M3(x 2^e - hi). A bf16 x has
+// 8 significant bits, hi takes the top 4 and the remainder fits lo exactly
+// unless it falls below E4M3's subnormal step (elements 2^-9 times the row's
+// largest or smaller). Rows hi ‖ lo (2 x 128 B) go to qsplit, 2^-e to qinv
+// (8 floats per group; unused ones 0).
+template <int G>
+__global__ void __launch_bounds__(256) pa_qsplit_kernel(const DecodeParams p) {
+  griddep_launch_dependents();  // the split-KV grid may start its prologue
+  const int grp = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (grp < p.num_tokens * p.num_kv_heads) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const size_t row = (size_t)grp * G + h;  // token * Hq + kv * G + h
+      const uint2 raw4 = __ldg(reinterpret_cast<const uint2*>(p.q + row * kD) + lane);
+      const float2 a = bf16x2_to_float2(raw4.x), c = bf16x2_to_float2(raw4.y);
+      float mx = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(c.x), fabsf(c.y)));
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kAllLanes, mx, o));
+      // e = 7 - floor(log2 mx), from the exponent field (a zero row keeps e = 0)
+      int ex = 0;
+      if (mx > 0.f) {
+        ex = 7 - (((int)(__float_as_uint(mx) >> 23) & 0xff) - 127);
+        ex = ex < -120 ? -120 : (ex > 120 ? 120 : ex);
+      }
+      const float sc = __uint_as_float((uint32_t)(127 + ex) << 23);   // 2^e, exact
+      const float isc = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-e
+      const float x0 = a.x * sc, x1 = a.y * sc, x2 = c.x * sc, x3 = c.y * sc;
+      const uint16_t h01 = float2_to_e4m3x2(x0, x1), h23 = float2_to_e4m3x2(x2, x3);
+      const float2 f01 = e4m3x2_to_float2(h01), f23 = e4m3x2_to_float2(h23);
+      const uint16_t l01 = float2_to_e4m3x2(x0 - f01.x, x1 - f01.y);
+      const uint16_t l23 = float2_to_e4m3x2(x2 - f23.x, x3 - f23.y);
+      unsigned char* const dst = const_cast<unsigned char*>(p.qsplit) + row * 2 * kD;
+      reinterpret_cast<uint32_t*>(dst)[lane] = (uint32_t)h01 | ((uint32_t)h23 << 16);
+      reinterpret_cast<uint32_t*>(dst + kD)[lane] = (uint32_t)l01 | ((uint32_t)l23 << 16);
+      if (lane == 0) const_cast<float*>(p.qinv)[(size_t)grp * 8 + h] = isc;
+    }
+    if (lane >= G && lane < 8) const_cast<float*>(p.qinv)[(size_t)grp * 8 + lane] = 0.f;
+  }
+  // complete only after the preceding grid (the KV write, the planner or the
+  // prefill grid): a dependent that waits for this grid sees theirs too
+  griddep_wait();
 }
 
 // ---------------------------------------------------------------------------------------
@@ -806,47 +1050,77 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------
 namespace {
 
-template <int G>
+template <int G, bool F8>
 cudaError_t launch_tc_t(const DecodeParams& d, int grid, cudaStream_t s) {
   TcDecodeParams tp;
   tp.d = d;
-  // q as {64 dims, rows, 2 halves}: a box of 8 rows lands as [half][8 rows][128 B]
   const uint64_t qrows = (uint64_t)d.num_tokens * (uint64_t)d.num_q_heads;
-  const uint64_t qd[3] = {64, qrows, 2}, qs[2] = {kD * 2, 128};
-  const uint32_t qb[3] = {64, 8, 2};
-  // a cache as {64 dims, 8 rows, 2 halves, 8-row groups}: a box of 2 groups
-  // (one 16-key block) lands as [group][half][8 rows][128 B]
-  const uint64_t groups = (uint64_t)d.num_blocks * (uint64_t)d.num_kv_heads * (kBlockSize / 8);
-  const uint64_t cd[4] = {64, 8, 2, groups}, cs[3] = {kD * 2, 128, 8 * kD * 2};
-  const uint32_t cb[4] = {64, 8, 2, kBlockSize / 8};
-  if (!encode_tmap_bf16(&tp.tm_q, 3, d.q, qd, qs, qb) ||
-      !encode_tmap_bf16(&tp.tm_k, 4, d.k_cache, cd, cs, cb) ||
-      !encode_tmap_bf16(&tp.tm_v, 4, d.v_cache, cd, cs, cb))
-    return cudaErrorInvalidValue;
-  auto kern = pa_decode_tc_kernel<G>;
+  if constexpr (F8) {
+    // q' rows as {128 B, rows (256 B apart), hi / lo (128 B apart)}: a box of 8
+    // rows lands as [hi, lo][8 rows][128 B]
+    const uint64_t qd[3] = {128, qrows, 2}, qs[2] = {2 * kD, kD};
+    const uint32_t qb[3] = {128, 8, 2};
+    const uint64_t rows = (uint64_t)d.num_blocks * (uint64_t)d.num_kv_heads * kBlockSize;
+    const uint64_t cd[2] = {128, rows}, cs[1] = {kD};
+    const uint32_t cb[2] = {128, kBlockSize};
+    if (!encode_tmap_u8(&tp.tm_q, 3, d.qsplit, qd, qs, qb) ||
+        !encode_tmap_u8(&tp.tm_k, 2, d.k_cache, cd, cs, cb) ||
+        !encode_tmap_u8(&tp.tm_v, 2, d.v_cache, cd, cs, cb))
+      return cudaErrorInvalidValue;
+  } else {
+    // q as {64 dims, rows, 2 halves}: a box of 8 rows lands as [half][8 rows][128 B]
+    const uint64_t qd[3] = {64, qrows, 2}, qs[2] = {kD * 2, 128};
+    const uint32_t qb[3] = {64, 8, 2};
+    // a cache as {64 dims, 8 rows, 2 halves, 8-row groups}: a box of 2 groups
+    // (one 16-key block) lands as [group][half][8 rows][128 B]
+    const uint64_t groups = (uint64_t)d.num_blocks * (uint64_t)d.num_kv_heads * (kBlockSize / 8);
+    const uint64_t cd[4] = {64, 8, 2, groups}, cs[3] = {kD * 2, 128, 8 * kD * 2};
+    const uint32_t cb[4] = {64, 8, 2, kBlockSize / 8};
+    if (!encode_tmap_bf16(&tp.tm_q, 3, d.q, qd, qs, qb) ||
+        !encode_tmap_bf16(&tp.tm_k, 4, d.k_cache, cd, cs, cb) ||
+        !encode_tmap_bf16(&tp.tm_v, 4, d.v_cache, cd, cs, cb))
+      return cudaErrorInvalidValue;
+  }
+  auto kern = pa_decode_tc_kernel<G, F8>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<F8>::SMEM);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = TcSmem<F8>::SMEM;
   cfg.stream = s;
   // Programmatic launch: the grid starts when the preceding grid triggers
-  // (the KV write at its top for a self-planned batch; otherwise the planner
-  // or the tensor-core prefill grid, at their end).
+  // (the KV write or the query split at its top for a self-planned batch;
+  // otherwise the planner or the tensor-core prefill grid, at their end).
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tp);
+}
+
+template <int G>
+cudaError_t launch_qsplit_t(const DecodeParams& d, cudaStream_t s) {
+  const int groups = d.num_tokens * d.num_kv_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((groups + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pa_qsplit_kernel<G>, d);
 }
 
 }  // namespace
@@ -856,19 +1130,30 @@ int decode_tc_workers(int num_sms) {
 }
 
 bool decode_tc_supported(int head_dim, int group, bool f8, int key_start_blocks) {
-  return head_dim == kD && !f8 && key_start_blocks == 0 &&
+  (void)f8;
+  return head_dim == kD && key_start_blocks == 0 &&
          (group == 1 || group == 2 || group == 4 || group == 8);
 }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int group, int num_sms, cudaStream_t s,
-                             int* workers_out) {
+cudaError_t launch_decode_tc(const DecodeParams& p, int group, bool f8, int num_sms,
+                             cudaStream_t s, int* workers_out) {
   const int grid = decode_tc_workers(num_sms);
   *workers_out = grid;
   switch (group) {
-    case 1: return launch_tc_t<1>(p, grid, s);
-    case 2: return launch_tc_t<2>(p, grid, s);
-    case 4: return launch_tc_t<4>(p, grid, s);
-    case 8: return launch_tc_t<8>(p, grid, s);
+    case 1: return f8 ? launch_tc_t<1, true>(p, grid, s) : launch_tc_t<1, false>(p, grid, s);
+    case 2: return f8 ? launch_tc_t<2, true>(p, grid, s) : launch_tc_t<2, false>(p, grid, s);
+    case 4: return f8 ? launch_tc_t<4, true>(p, grid, s) : launch_tc_t<4, false>(p, grid, s);
+    case 8: return f8 ? launch_tc_t<8, true>(p, grid, s) : launch_tc_t<8, false>(p, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_qsplit(const DecodeParams& p, int group, cudaStream_t s) {
+  switch (group) {
+    case 1: return launch_qsplit_t<1>(p, s);
+    case 2: return launch_qsplit_t<2>(p, s);
+    case 4: return launch_qsplit_t<4>(p, s);
+    case 8: return launch_qsplit_t<8>(p, s);
   }
   return cudaErrorInvalidValue;
 }

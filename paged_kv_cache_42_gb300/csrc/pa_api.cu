@@ -393,12 +393,19 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   dp.header_out = pp.header;
   dp.merge_tasks = reinterpret_cast<int4*>(ws + lay.tasks_off);
   dp.max_workers = cap > 0 ? cap : kMaxDecodeWorkers;
+  dp.qsplit = ws + lay.qsplit_off;
+  dp.qinv = reinterpret_cast<const float*>(ws + lay.qinv_off);
   dp.err = d->err;
+  if (use_tc && kv_fp8) {  // the E4M3 tensor-core kernel takes the queries split
+    const cudaError_t e = launch_qsplit(dp, group, s);
+    g_launches.fetch_add(1);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+  }
   int launched_workers = 0;
   {
     TimerScope timer(2, s);
     const cudaError_t e =
-        use_tc ? launch_decode_tc(dp, group, d->num_sms, s, &launched_workers)
+        use_tc ? launch_decode_tc(dp, group, kv_fp8 != 0, d->num_sms, s, &launched_workers)
                : launch_decode(dp, head_dim, group, kv_fp8 != 0, d->num_sms, occ_cap, s,
                                &launched_workers);
     g_launches.fetch_add(1);

@@ -77,7 +77,11 @@ static_assert(sizeof(WsHeader) == 256, "header occupies the first 256 bytes");
 
 // Workspace carve-up, identical on host and device.
 struct WsLayout {
-  size_t header_off, units_off, tiles_off, raw_off, workers_off, tasks_off, partials_off, total;
+  size_t header_off, units_off, tiles_off, raw_off, workers_off, tasks_off, partials_off;
+  // E4M3 caches on the tensor-core split-KV kernel: each query row scaled by a
+  // power of two and split into two E4M3 terms (hi, lo: 2 x head_dim bytes),
+  // and the inverse scales, 8 floats per (token, kv head)
+  size_t qsplit_off, qinv_off, total;
   int slot_floats;  // floats per partial-result slot
 };
 
@@ -98,7 +102,9 @@ __host__ __device__ inline WsLayout ws_layout(int num_reqs, int num_tokens, int 
   l.tasks_off = l.workers_off + pa_align256(sizeof(int) * (size_t)kMaxDecodeWorkers);
   l.partials_off = l.tasks_off + pa_align256(sizeof(int4) * (size_t)kMaxDecodeWorkers);
   const size_t slots = (size_t)num_tokens * num_kv_heads + kMaxDecodeWorkers;
-  l.total = l.partials_off + pa_align256(sizeof(float) * (size_t)l.slot_floats * slots);
+  l.qsplit_off = l.partials_off + pa_align256(sizeof(float) * (size_t)l.slot_floats * slots);
+  l.qinv_off = l.qsplit_off + pa_align256((size_t)num_tokens * num_q_heads * 2 * head_dim);
+  l.total = l.qinv_off + pa_align256(sizeof(float) * 8 * (size_t)num_tokens * num_kv_heads);
   return l;
 }
 
@@ -209,6 +215,10 @@ struct DecodeParams {
   // workers the slicing uses: at most the launched ones (a smaller value
   // leaves the rest idle and gives every worker a longer slice)
   int max_workers;
+  // E4M3 caches on the tensor-core kernel: the split query rows and inverse
+  // scales (WsLayout::qsplit_off, qinv_off), written by launch_qsplit
+  const unsigned char* qsplit;
+  const float* qinv;
   unsigned long long* err;
 };
 
@@ -284,8 +294,12 @@ int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap);
 // takes the same plan, partial slots and merge tasks as launch_decode.
 bool decode_tc_supported(int head_dim, int group, bool f8, int key_start_blocks);
 int decode_tc_workers(int num_sms);
-cudaError_t launch_decode_tc(const DecodeParams& p, int group, int num_sms, cudaStream_t s,
-                             int* workers_out);
+cudaError_t launch_decode_tc(const DecodeParams& p, int group, bool f8, int num_sms,
+                             cudaStream_t s, int* workers_out);
+// E4M3 caches: split every query row for the tensor-core kernel (into
+// p.qsplit / p.qinv), as a programmatic dependent of the preceding grid that
+// completes only after it.
+cudaError_t launch_qsplit(const DecodeParams& p, int group, cudaStream_t s);
 
 // 2-D tiled tensor map (CUtensorMap, passed as void*) over a row-major bf16
 // matrix of `rows` rows of `inner` elements, `row_stride_bytes` apart, with a
@@ -298,6 +312,9 @@ bool encode_tmap_bf16_2d(void* tmap, const void* ptr, uint64_t inner, uint64_t r
 // order: a dimension may step inside another's extent); 128-byte swizzle.
 bool encode_tmap_bf16(void* tmap, int rank, const void* ptr, const uint64_t* dims,
                       const uint64_t* strides_bytes, const uint32_t* box);
+// The same over byte data (E4M3 codes).
+bool encode_tmap_u8(void* tmap, int rank, const void* ptr, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
 
 // Resident split-KV CTAs per SM: two suit long per-token key ranges (each
 // worker's slice stays long); the short suffixes of a cascade call run better

@@ -717,9 +717,10 @@ bool get_encoder() {
 }
 
 bool encode_bf16(CUtensorMap* m, int rank, const void* ptr, const cuuint64_t* dims,
-                 const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+                 const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                 CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr),
+  const CUresult r = g_encode(m, dtype, rank, const_cast<void*>(ptr),
                               dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -737,8 +738,9 @@ bool encode_tmap_bf16_2d(void* tmap, const void* ptr, uint64_t inner, uint64_t r
   return encode_bf16(static_cast<CUtensorMap*>(tmap), 2, ptr, dims, str, box);
 }
 
-bool encode_tmap_bf16(void* tmap, int rank, const void* ptr, const uint64_t* dims,
-                      const uint64_t* strides_bytes, const uint32_t* box) {
+namespace {
+bool encode_tmap_any(void* tmap, int rank, const void* ptr, const uint64_t* dims,
+                     const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapDataType dt) {
   if (!get_encoder() || rank < 1 || rank > 5) return false;
   cuuint64_t d[5], st[4];
   cuuint32_t b[5];
@@ -747,7 +749,19 @@ bool encode_tmap_bf16(void* tmap, int rank, const void* ptr, const uint64_t* dim
     b[i] = (cuuint32_t)box[i];
     if (i + 1 < rank) st[i] = (cuuint64_t)strides_bytes[i];
   }
-  return encode_bf16(static_cast<CUtensorMap*>(tmap), rank, ptr, d, st, b);
+  return encode_bf16(static_cast<CUtensorMap*>(tmap), rank, ptr, d, st, b, dt);
+}
+}  // namespace
+
+bool encode_tmap_bf16(void* tmap, int rank, const void* ptr, const uint64_t* dims,
+                      const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap_any(tmap, rank, ptr, dims, strides_bytes, box,
+                         CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+bool encode_tmap_u8(void* tmap, int rank, const void* ptr, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tmap_any(tmap, rank, ptr, dims, strides_bytes, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
 namespace {

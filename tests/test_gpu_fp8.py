@@ -136,9 +136,77 @@ def test_attention_fp8_sweep(i, scales):
     run(w, *scales, f"fp8 sweep {i} scales {scales}")
 
 
-def test_llama8b_decode_fp8_sampled():
+def test_llama8b_decode_fp8_every_row():
     w = wl.make_config(2)
-    run(w, 0.0113, 0.0127, "llama8b fp8", reqs=[0, 1, 17, 40, 63])
+    run(w, 0.0113, 0.0127, "llama8b fp8, all rows")
+
+
+def test_long_context_fp8_every_row():
+    w = wl.make_config(5)
+    run(w, 0.0113, 0.0127, "long context fp8, all rows")
+
+
+# ---------------------------------------------------------------------------
+# the tensor-core split-KV kernel over E4M3 codes (kind::f8f6f4: the queries
+# split into two E4M3 terms, P' = 256 p split likewise), forced onto every
+# group, and the CUDA-core kernel forced onto the groups it no longer takes
+# ---------------------------------------------------------------------------
+TC_CASES = [
+    # (ctx_lens, q_lens, Hq, Hkv)
+    ([0, 14, 15, 16, 31, 63, 64, 127, 128, 129], [1] * 10, 64, 8),  # seq_len edges, G 8
+    ([2000, 3, 511, 512, 4095], [1] * 5, 32, 8),                      # G 4
+    ([8, 55, 16, 32, 200, 1000], [1] * 6, 8, 8),                      # G 1
+    ([300, 0, 5000, 17], [1, 1, 1, 1], 16, 8),                        # G 2
+    ([0, 0, 10, 100, 250], [1, 2, 15, 7, 3], 8, 1),                   # short spans, G 8
+]
+
+
+@pytest.fixture
+def decode_tc_option():
+    yield binding.set_option
+    binding.set_option("decode_tc", 1)
+    binding.set_option("decode_max_workers", 0)
+
+
+@pytest.mark.parametrize("i", range(len(TC_CASES)))
+@pytest.mark.parametrize("tc", [0, 2])
+def test_attention_fp8_both_split_kv_kernels(i, tc, decode_tc_option):
+    ctx, ql, hq, hkv = TC_CASES[i]
+    w = wl.make_workload(ctx, ql, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                         seed=1160 + i, pool_factor=1.3)
+    decode_tc_option("decode_tc", tc)
+    run(w, 0.0113, 0.0127, f"fp8 split-KV kernel {tc} case {i}")
+
+
+def test_attention_fp8_tensor_core_running_max_and_splits(decode_tc_option):
+    # scores that grow along the sequence move the reference max (and rescale
+    # both column groups of O); capping the workers splits it over 5 parts
+    L0 = 1500
+    w = wl.make_workload([L0 - 1], [1], num_q_heads=8, num_kv_heads=1, head_dim=128, seed=1170)
+    w.q[...] = wl.to_bf16_bits(np.float32(1.0))
+    for p in range(L0 - 1):
+        w.k_cache[w.block_tables[0, p // 16], 0, p % 16, :] = wl.to_bf16_bits(
+            np.float32(0.05 * (p // 64)))
+    w.k_new[0] = wl.to_bf16_bits(np.float32(0.05 * ((L0 - 1) // 64)))
+    decode_tc_option("decode_tc", 2)
+    run(w, 0.03, 1.0, "fp8 tc running max")
+    decode_tc_option("decode_max_workers", 5)
+    run(w, 0.03, 1.0, "fp8 tc running max, 5 parts")
+
+
+def test_attention_fp8_extreme_query_rows(decode_tc_option):
+    # query rows with large, tiny and zero magnitudes: each row's power-of-two
+    # scale keeps its split exact
+    w = wl.make_workload([300, 700, 40], [1, 1, 1], num_q_heads=32, num_kv_heads=8,
+                         head_dim=128, seed=1171)
+    q = wl.bf16_bits_to_f32(w.q).copy()
+    q[0] *= 1e3
+    q[1, :8] *= 1e-4
+    q[2, 3] = 0.0
+    w.q = wl.to_bf16_bits(q.astype(np.float32))
+    w.scale = 1.0 / 128.0 / 30.0
+    decode_tc_option("decode_tc", 2)
+    run(w, 0.0113, 0.0127, "fp8 tc extreme q rows")
 
 
 def test_mixed_batch_fp8_sampled():
