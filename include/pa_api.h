@@ -334,14 +334,16 @@ pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event
 #define PA_OPT_DECODE_SELF_PLAN 1
 /*
  *   PA_OPT_DECODE_TC (default 1): which kernel runs the split-KV work (the
- *     decodes and the spans shorter than 16 tokens) at head_dim 128 over a
- *     bf16 cache, without a cascade prefix. 0: the CUDA-core kernel always.
- *     1: the tensor-core kernel for GQA groups of 4 or 8 query heads per KV
- *     head, where the CUDA cores' arithmetic per cached byte, not HBM, would
- *     set the pace; the CUDA-core kernel otherwise. 2: the tensor-core kernel
- *     for every supported group. Both give results within the attention
- *     tolerances of the exact result; they are not bit-identical to each
- *     other (P is rounded to bf16 for the tensor-core P.V product).
+ *     decodes and the spans shorter than 16 tokens) at head_dim 128. 0: the
+ *     CUDA-core kernel always. 1: the tensor-core kernel for GQA groups of 4
+ *     or 8 query heads per KV head, over a bf16 or an E4M3 cache, where the
+ *     CUDA cores' arithmetic per cached byte, not HBM, would set the pace;
+ *     the CUDA-core kernel otherwise and for a cascade's suffix pass. 2: the
+ *     tensor-core kernel wherever it applies (every group; cascade suffixes
+ *     over a bf16 cache). Both give results within the attention tolerances
+ *     of the exact result; they are not bit-identical to each other (the
+ *     tensor-core kernel rounds P to bf16, or over an E4M3 cache splits the
+ *     queries and 256 P into two E4M3 terms each, for its products).
  *   PA_OPT_DECODE_MAX_WORKERS (default 0, no cap): at most this many
  *     split-KV workers share the flattened (token, kv head, block) work, so
  *     a long sequence is split over fewer parts (1: none). For tests of the

@@ -106,5 +106,36 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     return LIB_PATH
 
 
+def build_variant(name: str, defines: list) -> str:
+    """Build the library with extra preprocessor definitions into its own
+    directory and file (``lib<name>.so`` beside the library), leaving the
+    library itself untouched. For tests that need a differently configured
+    build; the variant is never loaded by the package."""
+    out_dir = os.path.join(PKG, "_build_" + name)
+    lib = os.path.join(PKG, f"lib{name}.so")
+    os.makedirs(out_dir, exist_ok=True)
+    flags = [f"-D{d}" for d in defines]
+
+    def one(src):
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
+        if src.endswith(".cpp"):
+            cmd = [cxx(), *HOST_FLAGS, "-c", src, "-o", obj]
+        else:
+            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"build of {name} failed for {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    srcs = _sources()
+    with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
+        objs = list(ex.map(one, srcs))
+    r = subprocess.run([nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", lib, *objs],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link of {name} failed:\n{r.stdout}\n{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))

@@ -46,6 +46,14 @@ constexpr unsigned kFull = 0xffffffffu;
 // =============================================================================
 // Split-KV decode kernel
 // =============================================================================
+// Test builds only: bytes added to every stage's expected transaction count,
+// so no stage barrier ever completes and the bounded waits give up (the
+// copies issued still land; see tests/test_gpu_wait_timeout.py). 0 in the
+// library.
+#ifndef PA_TEST_EXTRA_TX
+#define PA_TEST_EXTRA_TX 0
+#endif
+
 // Largest head group whose P.V pass gives each lane 8 output dims (else 4).
 // Eight dims halve the per-row overhead (address, p broadcast) of the pass at
 // the price of twice the accumulator registers (measured on the Llama-8B
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
       const uint32_t bar = bars + 8 * stage;
       const size_t off = ((size_t)pid * Hkv + kv) * (kBlockSize * D) * C::EB;  // bytes
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, 2 * C::KV_BYTES + (with_q ? C::Q_BYTES : 0));
+      mbar_arrive_expect_tx(bar, 2 * C::KV_BYTES + (with_q ? C::Q_BYTES : 0) + PA_TEST_EXTRA_TX);
       bulk_g2s(dst, static_cast<const unsigned char*>(p.k_cache) + off, C::KV_BYTES, bar);
       bulk_g2s(dst + C::KV_BYTES, static_cast<const unsigned char*>(p.v_cache) + off, C::KV_BYTES,
                bar);

@@ -423,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gb + M::OFF_TSLOT);
 
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
+  const int kstart = p.key_start_blocks;  // blocks of a cascade's common prefix, skipped here
   const int w = (int)blockIdx.x;
   const int all = (int)gridDim.x < p.max_workers ? (int)gridDim.x : p.max_workers;
   const int NW = W > 0 ? plan_workers(W, all) : 0;
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       k = lo;
       U = load_unit(k);
       Un = load_unit(k + 1);
-      nb = (U.len + kBlockSize - 1) / kBlockSize;
+      nb = max(1, (U.len + kBlockSize - 1) / kBlockSize - kstart);
       const int off = S - U.base;
       kv = off / nb;
       blk = off - kv * nb;
@@ -507,14 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = np & 1;
         const bool seg_done = blk + n == nb;
         const bool last = seg_done || y + n == E;
-        const SlotRec sr{U.tok, kv, blk * kBlockSize, U.len, t.nblk * kBlockSize, n * kBlockSize,
+        const SlotRec sr{U.tok, kv, (kstart + blk) * kBlockSize, U.len, t.nblk * kBlockSize,
+                         n * kBlockSize,
                          F_ACTIVE | (pfirst ? F_FIRST : 0) | (last ? F_LAST : 0) |
                              ((last && seg_done && pstart == 0) ? F_WHOLE : 0),
                          0};
         if (j == 0) t.s[0] = sr; else t.s[1] = sr;
         if (seg_done) t.last_blk = 1;
         if (lane >= t.nblk && lane < t.nblk + n) {
-          t.pid = __ldg(p.block_tables + (size_t)U.req * p.bt_stride + blk + (lane - t.nblk));
+          t.pid = __ldg(p.block_tables + (size_t)U.req * p.bt_stride + kstart + blk + (lane - t.nblk));
           t.kvl = kv;
         }
         pfirst = false;
@@ -535,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               U = Un;
               Un = load_unit(k + 1);
             } while (U.len <= 0);
-            nb = (U.len + kBlockSize - 1) / kBlockSize;
+            nb = max(1, (U.len + kBlockSize - 1) / kBlockSize - kstart);
           }
         }
       }
@@ -693,9 +695,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ns;
           }
           spins = 0;
-        } else if (++spins > 64) {  // nothing ready: give up after ~2 s without progress
+        } else if (++spins > 64) {  // nothing ready: give up after PA_WAIT_LIMIT_NS without progress
           if (spins == 65) t0 = global_timer_ns();
-          if (global_timer_ns() - t0 > 2000000000ull) {
+          if (global_timer_ns() - t0 > PA_WAIT_LIMIT_NS) {
             report_error(p.err, PA_DEVERR_WAIT_TIMEOUT, 2000 + M::B_PREADY);
             break;
           }
@@ -959,6 +961,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (rc.flags & F_WHOLE) {
+            float mh[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) mh[h] = mref[j][h];
+            // Cascade: the prefix partials of this (token, kv head), one per
+            // key chunk, folded in by log-sum-exp renormalisation.
+#pragma unroll 1
+            for (int c = 0; c < p.prefix_chunks; ++c) {
+              const float* const sl =
+                  p.prefix_partials + (((size_t)c * p.num_tokens + rc.tok) * Hkv + rc.kv) * p.slot_floats;
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                const float mc = __ldcg(sl + h);
+                const float mn = fmaxf(mh[h], mc);
+                const float a = exp2f(mh[h] - mn), bb = exp2f(mc - mn);
+                ls[h] = ls[h] * a + __ldcg(sl + G + h) * bb;
+                o[h] = o[h] * a + __ldcg(sl + 16 + h * kD + m) * bb;
+                mh[h] = mn;
+              }
+            }
             uint16_t* const orow = p.out + ((size_t)rc.tok * Hq + (size_t)rc.kv * G) * kD + m;
 #pragma unroll
             for (int h = 0; h < G; ++h) orow[h * kD] = bf16_bits(o[h] * (p.v_scale / ls[h]));
@@ -1130,8 +1151,8 @@ int decode_tc_workers(int num_sms) {
 }
 
 bool decode_tc_supported(int head_dim, int group, bool f8, int key_start_blocks) {
-  (void)f8;
-  return head_dim == kD && key_start_blocks == 0 &&
+  (void)key_start_blocks;  // a cascade's suffix pass (bf16 only: no E4M3 cascade)
+  return head_dim == kD && !(f8 && key_start_blocks > 0) &&
          (group == 1 || group == 2 || group == 4 || group == 8);
 }
 

@@ -87,8 +87,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait on a barrier phase: gives up after ~2 s of device time and
-// returns false, so a lost copy can never hang the GPU.
+// Device time after which a bounded wait gives up. The library waits 2 s; a
+// test build of the library shortens it to exercise the give-up path.
+#ifndef PA_WAIT_LIMIT_NS
+#define PA_WAIT_LIMIT_NS 2000000000ull
+#endif
+
+// Bounded wait on a barrier phase: gives up after PA_WAIT_LIMIT_NS of device
+// time and returns false, so a lost copy can never hang the GPU.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
 #pragma unroll 1
   for (int i = 0; i < 32; ++i)
@@ -97,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 #pragma unroll 1
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > 2000000000ull) return false;
+    if (global_timer_ns() - t0 > PA_WAIT_LIMIT_NS) return false;
   }
 }
 
