@@ -76,7 +76,8 @@
 //                    relative error near 2^-8, as bf16's); O^T keeps the two
 //                    column groups apart until the epilogue.
 // An E4M3 block is one 2 KB copy per tensor ([16 keys][128 B] rows are
-// already the swizzle width), a stage 37 KB, five stages.
+// already the swizzle width), a stage 36 KB, five stages. A stage is sent a
+// portion's q' rows only when it does not hold them already.
 //
 // Warp roles (192 threads, one CTA per SM): warps 0-3 softmax and epilogue
 // (warp w reads TMEM lanes 32w .. 32w+31), warp 4 the TMA producer (it also
@@ -128,8 +129,8 @@ struct TcL<false> {
   static constexpr uint32_t kTmemCols = 64;
 };
 // E4M3 cache. A K or V tile: [128 keys][128 B] (one 2 KB copy per block);
-// the q' operand: [2 slots][hi, lo][8 rows][128 B], then 1/2^e as [2 slots][8]
-// floats; P'^T: [32 rows][128 B]. N = 32: slot s is rows / columns 16 s ..,
+// the q' operand: [2 slots][hi, lo][8 rows][128 B] (1/2^e travels in the tile
+// record); P'^T: [32 rows][128 B]. N = 32: slot s is rows / columns 16 s ..,
 // the hi terms first.
 template <>
 struct TcL<true> {
@@ -137,7 +138,7 @@ struct TcL<true> {
   static constexpr int kGroup = 1024;
   static constexpr int kHalfOff = 0;
   static constexpr int kKvTile = 16384;
-  static constexpr int kQBytes = 4096 + 1024;
+  static constexpr int kQBytes = 4096;
   static constexpr int kN = 32;
   static constexpr int kSlotCols = 16;
   static constexpr int kKStep = 32;
@@ -157,7 +158,11 @@ struct TcSmem {
   static constexpr int OFF_STAGE = 0;
   static constexpr int OFF_P = L::kStages * kStageBytes;    // kSP buffers of P^T
   static constexpr int OFF_REC = OFF_P + kSP * L::kPBytes;  // one tile record per stage
-  static constexpr int OFF_XCH = OFF_REC + L::kStages * 64;  // [2][4 warps][16] floats
+  // E4M3: per stage, the inverse query scales of the tile's two slots ([2][8]
+  // floats), and which portion's q' rows each stage holds per slot
+  static constexpr int OFF_INV = OFF_REC + L::kStages * 64;
+  static constexpr int OFF_QTAG = OFF_INV + L::kStages * 64;
+  static constexpr int OFF_XCH = OFF_QTAG + 64;  // [2][4 warps][16] floats
   static constexpr int OFF_BAR = OFF_XCH + 2 * 4 * 16 * 4;
   // barriers: FULL[stages], EMPTY[stages], S[kSP], P_READY[kSP], P_FREE[kSP], XCH[2], DRAIN
   static constexpr int B_FULL = 0, B_EMPTY = L::kStages, B_S = 2 * L::kStages,
@@ -208,15 +213,6 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-// 1-D bulk copy global -> shared (16-byte aligned, multiple of 16 bytes).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 
 // TMEM loads/stores of N consecutive 32-bit columns of the warp's 32 lanes.
 template <int N>
@@ -491,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nblk;      // blocks in the tile; 0: no more tiles
       int last_blk;  // the tile holds a portion's last block (a decode's newest token)
       int pid, kvl;  // this lane's block id (loaded now, used two tiles later) and kv head
+      float invl;    // E4M3: lanes 8 j + h hold slot j's inverse query scale of head h
     };
     // The next tile: up to eight consecutive positions of the slice, from at
     // most two portions.
@@ -500,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       t.last_blk = 0;
       t.pid = 0;
       t.kvl = 0;
+      t.invl = 0.f;
 #pragma unroll
       for (int j = 0; j < 2; ++j) t.s[j] = SlotRec{0, 0, 0, 0, 0, 0, 0, 0};
       int used = 0;  // portions placed
@@ -515,6 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                          0};
         if (j == 0) t.s[0] = sr; else t.s[1] = sr;
         if (seg_done) t.last_blk = 1;
+        if (F8 && (lane >> 3) == j)
+          t.invl = __ldg(p.qinv + ((size_t)U.tok * Hkv + kv) * 8 + (lane & 7));
         if (lane >= t.nblk && lane < t.nblk + n) {
           t.pid = __ldg(p.block_tables + (size_t)U.req * p.bt_stride + kstart + blk + (lane - t.nblk));
           t.kvl = kv;
@@ -546,6 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int i = 0;
     bool ok = true;
+    int* const qtag = reinterpret_cast<int*>(gb + M::OFF_QTAG);
+    if (F8) {
+      if (lane < 2 * kStages) qtag[lane] = -1;
+      __syncwarp();
+    }
     // Issue one tile (cur) after computing the tile two ahead into nxt2; the
     // loop below rotates three descriptors at compile time instead of
     // copying them every tile (the producer's instructions are on the
@@ -567,14 +572,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++i;
         return false;
       }
-      const int nq = ((cur.s[0].flags & F_ACTIVE) ? 1 : 0) + ((cur.s[1].flags & F_ACTIVE) ? 1 : 0);
+      // the query-operand rows to copy: every active slot's (bf16), or (E4M3)
+      // those this stage does not hold yet
+      bool needq[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        needq[j] = (cur.s[j].flags & F_ACTIVE) != 0;
+        if (F8 && needq[j]) needq[j] = qtag[2 * st + j] != cur.s[j].tok * Hkv + cur.s[j].kv;
+      }
+      const int nq = (needq[0] ? 1 : 0) + (needq[1] ? 1 : 0);
+      if (F8 && lane < 16) reinterpret_cast<float*>(gb + M::OFF_INV + st * 64)[lane] = cur.invl;
+      __syncwarp();
       if (lane == 0) {
         recs[st].s[0] = cur.s[0];
         recs[st].s[1] = cur.s[1];
-        // per block: K and V (4 KB each bf16, 2 KB each E4M3); per active
-        // slot: its 8 query-operand rows (2 KB), and E4M3's 32 B of scales
-        mbar_arrive_expect_tx(full, (uint32_t)cur.nblk * (F8 ? 4096u : 8192u) +
-                                        (uint32_t)nq * (F8 ? 2048u + 32u : 2048u));
+        if (F8) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            if (needq[j]) qtag[2 * st + j] = cur.s[j].tok * Hkv + cur.s[j].kv;
+        }
+        // per block: K and V (4 KB each bf16, 2 KB each E4M3); per slot
+        // copied: its 8 query-operand rows (2 KB)
+        mbar_arrive_expect_tx(full, (uint32_t)cur.nblk * (F8 ? 4096u : 8192u) + (uint32_t)nq * 2048u);
       }
       __syncwarp();
       // a decode's newest token, written by the preceding grid, sits in its
@@ -600,8 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(sbase + L::kKvTile + lane * 2 * L::kGroup, &tp.tm_v, 0, 0, 0, grp, full);
         }
       }
-      const int qflags = lane == 0 ? cur.s[0].flags : cur.s[1].flags;
-      if (lane < 2 && (qflags & F_ACTIVE)) {  // the query operand rows of slot `lane`
+      if (lane < 2 && (lane == 0 ? needq[0] : needq[1])) {  // the query operand rows of slot `lane`
         const int qtok = lane == 0 ? cur.s[0].tok : cur.s[1].tok;
         const int qkv = lane == 0 ? cur.s[0].kv : cur.s[1].kv;
         // 8 rows from the group's first (rows past the group are other
@@ -609,9 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // unused columns)
         tma_load_3d(sbase + 2 * L::kKvTile + lane * 2048, &tp.tm_q, 0, qtok * Hq + qkv * G, 0,
                     full);
-        if constexpr (F8)  // the group's 8 inverse scales
-          bulk_load(sbase + 2 * L::kKvTile + 4096 + lane * 32,
-                    p.qinv + ((size_t)qtok * Hkv + qkv) * 8, 32, full);
       }
       ++i;
       return true;
@@ -800,8 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tm_ld<G>(trow + scol, shi);
           tm_ld<G>(trow + scol + 8, slo);
           tmem_wait_ld();
-          const float* const inv = reinterpret_cast<const float*>(
-              gb + M::OFF_STAGE + st * M::kStageBytes + 2 * L::kKvTile + 4096 + jj * 32);
+          const float* const inv = reinterpret_cast<const float*>(gb + M::OFF_INV + st * 64 + jj * 32);
 #pragma unroll
           for (int h = 0; h < G; ++h)
             t[h] = mine ? (__uint_as_float(shi[h]) + __uint_as_float(slo[h])) * (inv[h] * p.scale_log2)
