@@ -402,8 +402,15 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
 
 
 def time_kernels(res: Resident, steps: int, warmup: int, flush, torch, binding, dist) -> dict:
-    """Kernel durations (decode / tensor-core) from a separate timed pass."""
-    t = time_steps(res, steps, warmup, flush, torch, binding, dist, timers=True)
+    """Kernel durations (decode / tensor-core) from a separate timed pass.
+    The events around each launch serialise the grids, so a mixed batch is
+    timed here with the prefill / split-KV overlap off: every kernel on the
+    whole GPU, one after the other."""
+    binding.set_option("mixed_overlap", 0)
+    try:
+        t = time_steps(res, steps, warmup, flush, torch, binding, dist, timers=True)
+    finally:
+        binding.set_option("mixed_overlap", 1)
     return {"decode_ms": max_over_ranks(t["decode_ms"], dist),
             "prefill_ms": max_over_ranks(t["prefill_ms"], dist)}
 
@@ -572,6 +579,13 @@ def run_ours(args, rank, world, local, dist):
         entry = {"w": w, "sb": sb, "t": t, "ms": ms, "dec_ms": dec_ms, "pre_ms": pre_ms,
                  "res": res, "steps": steps, "signature": res.signature}
         entry["graph_ms"] = graph_steps(res, steps, args.warmup, flush, torch, dist)
+        if idx == MIXED_CONFIG:  # the same step with the chunks and split-KV work in turn
+            binding.set_option("mixed_overlap", 0)
+            try:
+                ts = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
+            finally:
+                binding.set_option("mixed_overlap", 1)
+            entry["serial_ms"] = max_over_ranks(ts["ms_per_step"], dist)
         if idx == args.config and not args.no_e2e:
             te = time_steps(res, max(20, steps // 4), args.warmup, flush, torch, binding, dist,
                             e2e=True)
@@ -642,10 +656,14 @@ def run_ours(args, rank, world, local, dist):
             "value": round(world * mw.num_tokens / (m["ms"] * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(m["ms"], 5), "steps": m["steps"],
             "step_signature": m["signature"],
+            "serial_ms_per_step": round(m["serial_ms"], 5),
+            "overlap": "prefill chunks on a few SMs beside the split-KV work (the planner's "
+                       "split); serial_ms_per_step: the two in turn on every SM",
             "cuda_graph_ms_per_step": round(m["graph_ms"], 5),
             "cuda_graph_value": round(world * mw.num_tokens / (m["graph_ms"] * 1e-3), 1),
             "attention_kernel_ms": round(m["dec_ms"], 5),
             "prefill_kernel_ms": round(m["pre_ms"], 5),
+            "kernel_ms_note": "kernels timed one after the other on every SM (overlap off)",
             "prefill_tflops": round(prefill_flops(mw) / (m["pre_ms"] * 1e-3) / 1e12, 1)
             if m["pre_ms"] > 0 else None,
             "kv_bytes": m["sb"]["kv"], "prefill_causal_flops": prefill_flops(mw)}

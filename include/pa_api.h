@@ -348,9 +348,22 @@ pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event
  *     split-KV workers share the flattened (token, kv head, block) work, so
  *     a long sequence is split over fewer parts (1: none). For tests of the
  *     split-count invariance; the default uses every worker the launch has.
+ *   PA_OPT_MIXED_OVERLAP (default 1): in a call with prefill chunks and
+ *     split-KV work on the tensor-core split-KV kernel (bf16 cache), the
+ *     planner may give the chunks a few SMs and the split-KV work the rest,
+ *     so that both run at once (the mixed batch of "vLLM v1 Deep Dive",
+ *     Part 3, Step 4c, whose prefill and decode spans one forward serves
+ *     together). It does so when its cost
+ *     model (per-SM prefill and split-KV rates measured on GB300) puts the
+ *     two ending together sooner than one after the other, and otherwise runs
+ *     them in turn as with the option off. The chunks' results are
+ *     bit-identical either way; the split-KV results stay within the
+ *     attention tolerances (fewer workers slice the keys differently).
+ *     value 0 turns it off.
  */
 #define PA_OPT_DECODE_TC 2
 #define PA_OPT_DECODE_MAX_WORKERS 3
+#define PA_OPT_MIXED_OVERLAP 4
 pa_status pa_set_option(int option, int value);
 
 /* Number of kernel launches the library has issued in this process. */

@@ -407,6 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     units = su;
     W = carry;
     K = R;
+  } else if (p.overlap) {
+    // started by the prefill-chunk grid once it had read the plan: the
+    // planner and the KV write before it are complete; this grid waits for
+    // the prefill-chunk grid only before it completes (see the end)
+    waited = true;
+    W = __ldcg(&p.header->num_positions);
+    K = __ldcg(&p.header->num_units);
   } else {
     griddep_wait();  // the plan is written by the preceding grid
     waited = true;
@@ -421,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
   const int kstart = p.key_start_blocks;  // blocks of a cascade's common prefix, skipped here
   const int w = (int)blockIdx.x;
-  const int all = (int)gridDim.x < p.max_workers ? (int)gridDim.x : p.max_workers;
+  int all = (int)gridDim.x < p.max_workers ? (int)gridDim.x : p.max_workers;
+  if (p.overlap) all = min(all, __ldcg(&p.header->decode_workers));
   const int NW = W > 0 ? plan_workers(W, all) : 0;
   int S = 0, E = 0;
   if (w < NW) {
@@ -431,8 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // ======================= work walk + TMA producer =======================
+    // the planner's table (global memory, written by an earlier grid) is read
+    // from L2; a self-planned one sits in shared memory
     auto load_unit = [&](int k) -> UnitInfo {
-      const int4 u = *reinterpret_cast<const int4*>(units + k);
+      const int4 u = p.self_plan ? *reinterpret_cast<const int4*>(units + k)
+                                 : __ldcg(reinterpret_cast<const int4*>(units + k));
       return UnitInfo{u.x, u.y, u.z, u.w};
     };
     // the walk: the portion holding position y is (unit k, kv head kv), at
@@ -444,14 +455,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (S < E) {
       int lo = 0, hi = K;  // base[lo] <= S < base[hi]
       if (p.worker_unit && !p.self_plan) {
-        lo = __ldg(p.worker_unit + w);
+        lo = __ldcg(p.worker_unit + w);
         hi = lo + 1;
       }
 #pragma unroll 1
       while (hi - lo > 1) {
         const int step = (hi - lo + 31) / 32;
         const int idx = lo + lane * step;
-        const bool ok = idx < hi && units[idx].base <= S;
+        const bool ok = idx < hi && load_unit(idx).base <= S;
         const unsigned bal = __ballot_sync(kAllLanes, ok);
         lo = lo + (31 - __clz(bal)) * step;
         hi = min(hi, lo + step);
@@ -1033,6 +1044,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
+  // overlapped mixed batch: complete only after the prefill-chunk grid, so
+  // that whoever waits for this grid (the merge pass, later work on the
+  // stream) sees the whole call
+  if (p.overlap && threadIdx.x == 0) griddep_wait();
 }
 
 // One warp per (token, kv head): each of the G query rows is scaled by the

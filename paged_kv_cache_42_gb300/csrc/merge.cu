@@ -37,7 +37,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
   const int W = __ldcg(&p.header->num_positions);
   const int4 task = __ldcg(p.tasks + w);
   // tasks past this call's worker count are stale
-  if (W <= 0 || w >= plan_workers(W, p.num_workers) || task.x < 0) return;
+  int nw = p.num_workers;
+  if (p.workers_from_header) nw = min(nw, __ldcg(&p.header->decode_workers));
+  if (W <= 0 || w >= plan_workers(W, nw) || task.x < 0) return;
   const int tok = task.x, kv = task.y, wf = task.z, wl = task.w;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 

@@ -40,6 +40,7 @@ std::atomic<long long> g_launches{0};
 std::atomic<int> g_self_plan{1};  // pa_set_option(PA_OPT_DECODE_SELF_PLAN, ...)
 std::atomic<int> g_decode_tc{1};  // pa_set_option(PA_OPT_DECODE_TC, ...): 0 off, 1 auto, 2 on
 std::atomic<int> g_max_workers{0};  // pa_set_option(PA_OPT_DECODE_MAX_WORKERS, ...): 0 = no cap
+std::atomic<int> g_mixed_overlap{1};  // pa_set_option(PA_OPT_MIXED_OVERLAP, ...)
 constexpr int kNumTimers = 6;  // write, plan, decode, prefill, cascade prefix, merge
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
@@ -321,6 +322,13 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   if (launched <= 0) return PA_ERR_CUDA;
   const int cap = g_max_workers.load();
   pp.num_workers = (cap > 0 && cap < launched) ? cap : launched;
+  // A mixed batch on the tensor-core split-KV kernel (bf16) may run its
+  // prefill chunks on a few SMs beside the split-KV work (the planner decides
+  // how many, or none); the E4M3 path keeps its query-split pass between them.
+  const int overlap = (g_mixed_overlap.load() && pp.use_prefill && use_tc && !kv_fp8) ? 1 : 0;
+  pp.overlap = overlap;
+  pp.num_sms = d->num_sms;
+  pp.position_bytes = 2 * kBlockSize * head_dim * 2;  // K and V of one 16-key block
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
   pp.units = reinterpret_cast<UnitInfo*>(ws + lay.units_off);
   pp.tiles = reinterpret_cast<PrefillTile*>(ws + lay.tiles_off);
@@ -358,6 +366,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
     pl.num_blocks = num_blocks;
     pl.bt_stride = max_blocks_per_req;
     pl.scale_log2 = scale * 1.4426950408889634f * (kv_fp8 ? k_scale : 1.f);
+    pl.overlap = overlap;
     pl.err = d->err;
     TimerScope timer(prefix_len > 0 ? 4 : 3, s);
     const cudaError_t e = launch_prefill(pl, d->num_sms, s);
@@ -399,6 +408,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   dp.max_workers = cap > 0 ? cap : kMaxDecodeWorkers;
   dp.qsplit = ws + lay.qsplit_off;
   dp.qinv = reinterpret_cast<const float*>(ws + lay.qinv_off);
+  dp.overlap = overlap;
   dp.err = d->err;
   if (use_tc && kv_fp8) {  // the E4M3 tensor-core kernel takes the queries split
     const cudaError_t e = launch_qsplit(dp, group, s);
@@ -424,6 +434,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   mp.partials = dp.partials;
   mp.slot_floats = lay.slot_floats;
   mp.num_workers = workers;
+  mp.workers_from_header = overlap;
   mp.num_q_heads = num_q_heads;
   mp.num_kv_heads = num_kv_heads;
   mp.num_tokens = num_tokens;
@@ -526,6 +537,9 @@ pa_status pa_set_option(int option, int value) {
     case PA_OPT_DECODE_TC:
       if (value < 0 || value > 2) return PA_ERR_INVALID_ARG;
       g_decode_tc.store(value);
+      return PA_OK;
+    case PA_OPT_MIXED_OVERLAP:
+      g_mixed_overlap.store(value ? 1 : 0);
       return PA_OK;
     case PA_OPT_DECODE_MAX_WORKERS:
       if (value < 0) return PA_ERR_INVALID_ARG;

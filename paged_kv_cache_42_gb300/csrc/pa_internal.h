@@ -56,8 +56,25 @@ struct WsHeader {
   int num_units;      // K: tokens with work on the split-KV path
   int num_positions;  // W: sum over units of Hkv * ceil(len / 16)
   int num_tiles;      // prefill-chunk tiles for the tensor-core path
-  int pad[61];
+  // Overlapped mixed batch (PlanParams::overlap): CTAs of the prefill-chunk
+  // grid that take items (the rest retire at once), and split-KV workers.
+  // Otherwise prefill_ctas is the whole grid's share and decode_workers the
+  // launch's worker count.
+  int prefill_ctas;
+  int decode_workers;
+  int pad[59];
 };
+
+// Overlapped mixed batch: the planner gives the prefill-chunk items P SMs
+// and the split-KV work the other S - P, when the two then end together
+// sooner than one after the other. Costs, measured on GB300 at head_dim 128:
+// one prefill step (two 128-row tiles against 128 keys) holds an SM for
+// about kPrefillStepUs; the split-KV kernel streams about kDecodeSmBytesPerUs
+// per SM until the copy peak (kHbmBytesPerUs) caps it.
+constexpr float kPrefillStepUs = 2.4f;
+constexpr float kDecodeSmBytesPerUs = 47.0e3f;
+constexpr float kHbmBytesPerUs = 6.6e6f;
+constexpr float kOverlapMargin = 0.85f;  // prefill share planned to end this early
 
 // Requests with at least this many new tokens go to the tensor-core
 // prefill-chunk kernel; shorter ones (decodes, short verify spans) to the
@@ -154,6 +171,10 @@ struct PlanParams {
   int group;        // G = Hq / Hkv
   int use_prefill;  // route requests with qlen >= kPrefillMinQlen to the tensor-core kernel
   int num_workers;  // split-KV workers the decode launch provides
+  // overlapped mixed batch allowed: the planner may split the SMs between the
+  // prefill-chunk and split-KV grids (num_sms of them; position_bytes of
+  // K and V per split-KV position)
+  int overlap, num_sms, position_bytes;
   WsHeader* header;
   UnitInfo* units;
   PrefillTile* tiles;
@@ -183,6 +204,9 @@ struct PrefillLaunch {
   const PrefillTile* tiles;
   int num_tokens, num_q_heads, num_kv_heads, head_dim, num_blocks, bt_stride;
   float scale_log2;
+  // overlapped mixed batch: header->prefill_ctas CTAs take the items and the
+  // grid releases the split-KV grid as soon as it has read that count
+  int overlap;
   unsigned long long* err;
 };
 
@@ -219,6 +243,11 @@ struct DecodeParams {
   // scales (WsLayout::qsplit_off, qinv_off), written by launch_qsplit
   const unsigned char* qsplit;
   const float* qinv;
+  // overlapped mixed batch: this grid starts while the prefill-chunk grid
+  // still runs (its predecessor's predecessor, the planner, is complete);
+  // the worker count comes from the header and the grid completes only after
+  // the prefill-chunk grid
+  int overlap;
   unsigned long long* err;
 };
 
@@ -235,6 +264,7 @@ struct MergeParams {
   const float* partials;
   int slot_floats;
   int num_workers;  // split-KV workers launched (the slicing's upper bound)
+  int workers_from_header;  // overlapped mixed batch: header->decode_workers, if fewer
   int num_q_heads, num_kv_heads, num_tokens;
   int key_start_blocks;
   const float* prefix_partials;

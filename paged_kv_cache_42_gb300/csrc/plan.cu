@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   __shared__ long long scan_sm[32];
   __shared__ int bucket_cnt[kTileBuckets];
   __shared__ int bucket_pos[kTileBuckets];
+  __shared__ int s_steps;    // prefill steps (item x key tile) of the batch
+  __shared__ int s_workers;  // split-KV workers the slicing uses
   // Per-token scratch: {request, keys to attend}, then the compacted units'
   // first positions. In shared memory when the batch fits, else in the
   // workspace.
@@ -75,6 +77,7 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   if (p.use_prefill)
     for (int b = threadIdx.x; b < kTileBuckets; b += blockDim.x) bucket_cnt[b] = 0;
   for (int t = threadIdx.x; t < T; t += blockDim.x) raw[t] = make_int2(-1, 0);
+  if (threadIdx.x == 0) s_steps = 0;
   __syncthreads();
 
   // a request is valid when its span lies in [0, T] and its lengths agree
@@ -101,11 +104,27 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   };
 
   if (p.prefix_blocks > 0) {  // every table starts with request 0's prefix blocks
+    // kCheckBatch independent loads per thread before any compare: one DRAM
+    // round trip per batch rather than one per entry
+    constexpr int kCheckBatch = 8;
     const long long n = (long long)(p.num_reqs - 1) * p.prefix_blocks;
-    for (long long i = threadIdx.x; i < n; i += blockDim.x) {
-      const int r = 1 + (int)(i / p.prefix_blocks), b = (int)(i % p.prefix_blocks);
-      if (p.block_tables[(size_t)r * p.max_blocks_per_req + b] != p.block_tables[b])
-        report_error(p.err, PA_DEVERR_PREFIX, r);
+    for (long long i0 = threadIdx.x; i0 < n; i0 += (long long)kCheckBatch * blockDim.x) {
+      int got[kCheckBatch], want[kCheckBatch];
+#pragma unroll
+      for (int k = 0; k < kCheckBatch; ++k) {
+        const long long i = i0 + (long long)k * blockDim.x;
+        got[k] = want[k] = 0;
+        if (i < n) {
+          const int r = 1 + (int)(i / p.prefix_blocks), b = (int)(i % p.prefix_blocks);
+          got[k] = __ldg(p.block_tables + (size_t)r * p.max_blocks_per_req + b);
+          want[k] = __ldg(p.block_tables + b);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kCheckBatch; ++k)
+        if (got[k] != want[k])
+          report_error(p.err, PA_DEVERR_PREFIX,
+                       1 + (int)((i0 + (long long)k * blockDim.x) / p.prefix_blocks));
     }
   }
   for (int r = threadIdx.x; r < p.num_reqs; r += blockDim.x) {
@@ -113,8 +132,13 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     if (!check(r, q0, qlen, L, true)) continue;
     const int ctx = L - qlen;
     if (p.use_prefill && qlen >= kPrefillMinQlen) {
-      for (int j0 = 0; j0 < qlen; j0 += tok_per_item)
-        atomicAdd(&bucket_cnt[min(tile_nkv(L, ctx, j0), kTileBuckets - 1)], p.num_kv_heads);
+      int steps = 0;
+      for (int j0 = 0; j0 < qlen; j0 += tok_per_item) {
+        const int nkv = tile_nkv(L, ctx, j0);
+        atomicAdd(&bucket_cnt[min(nkv, kTileBuckets - 1)], p.num_kv_heads);
+        steps += nkv;
+      }
+      if (p.overlap) atomicAdd(&s_steps, steps * p.num_kv_heads);
       continue;  // these tokens are not on the split-KV path
     }
     for (int j = 0; j < qlen; ++j) raw[q0 + j] = make_int2(r, ctx + j + 1);
@@ -169,12 +193,39 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     if (ubase) ubase[K] = W;
     p.header->num_units = K;
     p.header->num_positions = W;
+    // Overlapped mixed batch: the fewest SMs c that finish the prefill steps
+    // (a margin ahead of) the split-KV work on the other S - c, if that beats
+    // running the two one after the other. The split-KV time on n SMs is
+    // bytes / min(n x per-SM rate, copy peak); the chunks alone on every SM
+    // end at about 1.6x their even share (the longest items set the end).
+    int ctas = p.num_sms, workers = p.num_workers;
+    if (p.overlap && p.use_prefill && W > 0 && s_steps > 0) {
+      const int S_ = p.num_sms;
+      const float pre = kPrefillStepUs * (float)s_steps;  // SM x us
+      const float bytes = (float)W * (float)p.position_bytes;
+      auto dec_us = [&](int n) {
+        return fmaxf(bytes / ((float)n * kDecodeSmBytesPerUs), bytes / kHbmBytesPerUs);
+      };
+      // smallest c with pre / c <= margin x dec_us(S - c), per branch of the max
+      const float c1 = pre * (float)S_ * kDecodeSmBytesPerUs /
+                       (kOverlapMargin * bytes + pre * kDecodeSmBytesPerUs);
+      const float c2 = pre * kHbmBytesPerUs / (kOverlapMargin * bytes);
+      const int c = max(1, (int)ceilf(fminf(fminf(c1, c2), (float)S_)));
+      const float serial = 1.6f * pre / (float)S_ + dec_us(S_);
+      if (c <= S_ / 4 && dec_us(S_ - c) < serial) {
+        ctas = c;
+        workers = min(workers, S_ - c);
+      }
+    }
+    p.header->prefill_ctas = ctas;
+    p.header->decode_workers = workers;
+    s_workers = workers;
   }
   // each split-KV worker's first unit (same worker count and slicing as the
   // split-KV kernel), found by binary search over the units' first positions
+  __syncthreads();
   if (ubase) {
-    __syncthreads();
-    const int NW = plan_workers(W, p.num_workers);
+    const int NW = plan_workers(W, s_workers);
     for (int w = threadIdx.x; w < NW; w += blockDim.x) {
       const int S = (int)((long long)w * W / NW);
       int lo = 0, hi = K;  // ubase[lo] <= S < ubase[hi]
@@ -215,7 +266,10 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
   // batch (fewer warps per barrier) plans it faster.
   int threads = kPlanThreads;
   if (!p.use_prefill) {
-    const int need = p.num_tokens > p.num_reqs ? p.num_tokens : p.num_reqs;
+    int need = p.num_tokens > p.num_reqs ? p.num_tokens : p.num_reqs;
+    // a cascade's prefix check reads (requests - 1) x prefix blocks entries
+    if (p.prefix_blocks > 0 && (long long)(p.num_reqs - 1) * p.prefix_blocks > need)
+      need = kPlanThreads;
     threads = need <= 128 ? 128 : need <= 256 ? 256 : need <= 512 ? 512 : kPlanThreads;
   }
   cfg.blockDim = dim3(threads);

@@ -149,6 +149,7 @@ struct PrefillParams {
   const unsigned char* k_cache8;
   const unsigned char* v_cache8;
   float v_scale;
+  int overlap;  // PrefillLaunch::overlap
   unsigned long long* err;
 };
 
@@ -225,12 +226,12 @@ __device__ __forceinline__ void widen_e4m3_row(const unsigned char* src, bool va
   }
 }
 
-// The r-th work item of this CTA. Items come sorted longest first; rounds of
-// gridDim.x items alternate direction (CTA b takes b, then 2g-1-b, then
+// The r-th work item of CTA blockIdx.x among the g CTAs that take items.
+// Items come sorted longest first; rounds of g items alternate direction (CTA b takes b, then 2g-1-b, then
 // 2g+b, ...), so a CTA that drew a long item in one round draws a short one
 // in the next instead of the next-longest.
-__device__ __forceinline__ int snake_item(int r) {
-  const int g = (int)gridDim.x, b = (int)blockIdx.x;
+__device__ __forceinline__ int snake_item(int r, int g) {
+  const int b = (int)blockIdx.x;
   return r * g + ((r & 1) ? g - 1 - b : b);
 }
 
@@ -272,8 +273,19 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
   // The work list comes from the preceding (planner) grid. The prefix pass
   // needs none of it and waits only before it completes (see the end).
   if constexpr (!PREFIX) griddep_wait();
-  const int ntiles =
-      PREFIX ? p.prefix_pairs * p.num_kv_heads * p.prefix_chunks : p.header->num_tiles;
+  int ntiles = PREFIX ? p.prefix_pairs * p.num_kv_heads * p.prefix_chunks : p.header->num_tiles;
+  // CTAs taking items: all, or (overlapped mixed batch) the planner's share;
+  // the others retire at once and leave their SMs to the split-KV grid,
+  // which every CTA releases here rather than on completion
+  int ctas = (int)gridDim.x;
+  if (!PREFIX && p.overlap) {
+    const int c = __ldcg(&p.header->prefill_ctas);
+    if (c > 0 && c < ctas) {
+      ctas = c;
+      griddep_launch_dependents();
+    }
+    if ((int)blockIdx.x >= ctas) ntiles = 0;
+  }
 
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8 * i; };
   auto wait = [&](int i, uint32_t parity) -> bool {
@@ -288,7 +300,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     // lanes 0..7 each copy one 16-key block.
     int g = 0, it = 0;
     bool ok = true;
-    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
+    for (int t = snake_item(it, ctas); ok && t < ntiles; t = snake_item(++it, ctas)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int nb = (tl.L + kBlockSize - 1) / kBlockSize;
       const int32_t* const bt_row = p.block_tables + (size_t)tl.req * p.bt_stride;
@@ -357,7 +369,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     int np[2] = {0, 0};  // P_t events consumed
     int it = 0;
     bool ok = true;
-    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
+    for (int t = snake_item(it, ctas); ok && t < ntiles; t = snake_item(++it, ctas)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int L = tl.L;
       if (!wait(B_Q_FULL, it & 1)) { ok = false; break; }
@@ -478,7 +490,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     };
     int ns = 0, it = 0;  // S_rt events consumed; work items done
     bool ok = true;
-    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
+    for (int t = snake_item(it, ctas); ok && t < ntiles; t = snake_item(++it, ctas)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int L = tl.L;
       int qlen = 0, j = 0, lim;
@@ -648,7 +660,7 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     const int r = threadIdx.x - kThreads;  // key row of the tile, 0..127 (converter warps)
     int g = 0, it = 0;
     bool ok = true;
-    for (int t = snake_item(it); ok && t < ntiles; t = snake_item(++it)) {
+    for (int t = snake_item(it, ctas); ok && t < ntiles; t = snake_item(++it, ctas)) {
       const Item tl = get_item<D, G, PREFIX>(p, t);
       const int32_t* const bt_row = p.block_tables + (size_t)tl.req * p.bt_stride;
       for (int i = 0; i < tl.n; ++i, ++g) {
@@ -805,6 +817,7 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
   p.k_cache8 = F8 ? static_cast<const unsigned char*>(a.k_cache) : nullptr;
   p.v_cache8 = F8 ? static_cast<const unsigned char*>(a.v_cache) : nullptr;
   p.v_scale = F8 ? a.v_scale : 1.f;
+  p.overlap = PREFIX ? 0 : a.overlap;
   int grid = num_sms;
   if (PREFIX) {
     const int items = p.prefix_pairs * a.num_kv_heads * a.prefix_chunks;
