@@ -25,9 +25,10 @@
 //                    tile and B = the G q rows, 128B-swizzled K-major in
 //                    shared memory; fp32 into TMEM (lane = key).
 //   softmax          one thread per key (its TMEM lane): mask, scale, the
-//                    tile's max over 128 keys (warp shuffles, then a 4-warp
-//                    exchange on an mbarrier), exp2; P^T rounded to bf16 into
-//                    shared memory in the B-operand layout.
+//                    tile's max over 128 keys where needed (warp shuffles,
+//                    then a 4-warp exchange on an mbarrier), exp2; P^T
+//                    rounded to bf16 into shared memory in the B-operand
+//                    layout.
 //   O^T += V^T P^T   M = 128 head dims, N = 16, K = 128 keys; A = the same V
 //                    tile image read M/N-major, B = P^T; O^T stays in TMEM
 //                    (lane = head dim) across the tiles of a (token, kv head),
@@ -70,9 +71,10 @@
 //                    kernel before this one (launch_qsplit). N = 32: per slot,
 //                    8 rows of hi then 8 of lo; the softmax adds the two
 //                    column groups and undoes 2^e.
-//   O^T += V^T P'^T  P' = 256 p against a reference max that moves whenever
-//                    a tile's max exceeds it by more than 0.75 (so P' <= 430,
-//                    inside E4M3's 448), split the same way into hi + lo (a
+//   O^T += V^T P'^T  P' = 256 p against a reference max, set 1 above the
+//                    maxima it comes from, that moves whenever a tile's max
+//                    exceeds it by more than 0.75 (so P' <= 430, inside
+//                    E4M3's 448), split the same way into hi + lo (a
 //                    relative error near 2^-8, as bf16's); O^T keeps the two
 //                    column groups apart until the epilogue.
 // An E4M3 block is one 2 KB copy per tensor ([16 keys][128 B] rows are
@@ -758,6 +760,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
+    // Whether any of the 128 threads holds v, on the same exchange: the
+    // warps' votes meet in the exchange buffer.
+    auto block_any = [&](bool v, bool& any) -> bool {
+      const bool wv = __any_sync(kAllLanes, v);
+      const int kx = nx++;
+      float* const xb = xch + (kx & 1) * 64;
+      if (lane == 0) xb[warp * 16 + 15] = wv ? 1.f : 0.f;
+      mbar_arrive(BAR(M::B_XCH + (kx & 1)));
+      if (!wait(M::B_XCH + (kx & 1), kx >> 1)) return false;
+      any = (xb[15] + xb[31]) + (xb[47] + xb[63]) != 0.f;
+      return true;
+    };
     // O^T starts at zero (the P.V MMAs always accumulate)
     {
       uint32_t z[8];
@@ -789,9 +803,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prow8 = [&](int b, int r) -> unsigned char* {
       return gb + M::OFF_P + b * L::kPBytes + r * 128 + ((((m >> 4) ^ (r & 7))) << 4) + (m & 15);
     };
+    // This thread's P^T entries of slot j in buffer b: bf16, or (E4M3)
+    // P' = 256 p as hi + lo, one byte per row of the slot
+    auto write_p = [&](int b, int j, const float (&pr)[G]) {
+      if constexpr (F8) {
+#pragma unroll
+        for (int h = 0; h < G; h += 2) {
+          const float x0 = 256.f * pr[h], x1 = h + 1 < G ? 256.f * pr[h + 1] : 0.f;
+          const uint16_t hi = float2_to_e4m3x2(x0, x1);
+          const float2 hf = e4m3x2_to_float2(hi);
+          const uint16_t lo = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
+          *prow8(b, 16 * j + h) = (unsigned char)(hi & 0xffu);
+          *prow8(b, 16 * j + 8 + h) = (unsigned char)(lo & 0xffu);
+          if (h + 1 < G) {
+            *prow8(b, 16 * j + h + 1) = (unsigned char)(hi >> 8);
+            *prow8(b, 16 * j + 8 + h + 1) = (unsigned char)(lo >> 8);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) *prow(b, j, h) = bf16_bits(pr[h]);
+      }
+    };
     // The reference max moves only when a tile's max exceeds it by more than
     // this (log2 units): 2^8 for bf16 P, 0.75 for E4M3 P' = 256 p <= 430.
     constexpr float kSlack = F8 ? 0.75f : 8.f;
+    // E4M3: a reference is set 1 (log2 units) above the maxima it is taken
+    // from, so it moves only for a score 1.75 above them (P' then peaks at
+    // 128 and loses one octave at the bottom, below 2^-16 of the maximum)
+    constexpr float kHead = F8 ? 1.f : 0.f;
     int i = 0;
     bool ok = true;
 #pragma unroll 1
@@ -838,57 +878,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < G; ++h) t[h] = mine ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
         }
-        float tm[G], mr[G], lt[G];
+        float mr[G], lt[G];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          tm[h] = t[h];
           mr[h] = jj ? mref[1][h] : mref[0][h];
           lt[h] = jj ? lth[1][h] : lth[0][h];
         }
-        if (!block_reduce(tm, true)) { ok = false; break; }
-        // reference maxima: a portion's first tile sets them (it holds the
+        // Reference maxima: a portion's first tile sets them (it holds the
         // portion's first key, so they are finite); later tiles move them
-        // only by more than kSlack, rescaling the slot's O^T columns
-        bool resc = false;
-        float alpha[G];
+        // only by more than kSlack, rescaling the slot's O^T columns. Where
+        // that is rare (bf16: P up to 2^8; E4M3 at G = 8) the threads first
+        // vote on whether any score is above its reference by that much, and
+        // only a tile the vote flags takes its maxima. (E4M3's slack is small:
+        // on the Llama-8B batch at G = 4 about one tile in four moves its
+        // reference, and the vote then costs a second exchange.)
+        constexpr bool kVote = !F8 || G == 8;
+        const bool first = (fl & F_FIRST) != 0;
+        bool need_max = first || !kVote;
+        if (!need_max) {
+          bool over = false;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          alpha[h] = 1.f;
-          if (fl & F_FIRST) {
-            mr[h] = tm[h];
-            lt[h] = 0.f;
-          } else if (tm[h] > mr[h] + kSlack) {
-            alpha[h] = exp2f(mr[h] - tm[h]);
-            mr[h] = tm[h];
-            resc = true;
-          }
+          for (int h = 0; h < G; ++h) over |= t[h] > mr[h] + kSlack;
+          if (!block_any(over, need_max)) { ok = false; break; }
         }
-        if (resc) {  // uniform: every thread holds the same maxima
-          // O^T is stable once the previous tile's P.V has completed
-          if (!wait(M::B_PFREE + (i - 1) % kSP, (i - 1) / kSP)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t ocol = M::kTmO + L::kSlotCols * jj;
+        if (need_max) {
+          float tm[G];
 #pragma unroll
-          for (int g = 0; g < L::kSlotCols; g += 8) {  // E4M3: the hi and the lo group
-            uint32_t o[G];
-            tm_ld<G>(trow + ocol + g, o);
-            tmem_wait_ld();
+          for (int h = 0; h < G; ++h) tm[h] = t[h];
+          if (!block_reduce(tm, true)) { ok = false; break; }
+          bool resc = false;
+          float alpha[G];
 #pragma unroll
-            for (int h = 0; h < G; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-            tm_st<G>(trow + ocol + g, o);
+          for (int h = 0; h < G; ++h) {
+            alpha[h] = 1.f;
+            if (first) {
+              mr[h] = tm[h] + kHead;
+              lt[h] = 0.f;
+            } else if (tm[h] > mr[h] + kSlack) {
+              alpha[h] = exp2f(mr[h] - (tm[h] + kHead));
+              mr[h] = tm[h] + kHead;
+              resc = true;
+            }
           }
-          tmem_wait_st();
+          if (resc) {  // uniform: every thread holds the same maxima
+            // O^T is stable once the previous tile's P.V has completed
+            if (!wait(M::B_PFREE + (i - 1) % kSP, (i - 1) / kSP)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ocol = M::kTmO + L::kSlotCols * jj;
 #pragma unroll
-          for (int h = 0; h < G; ++h) lt[h] *= alpha[h];
+            for (int g = 0; g < L::kSlotCols; g += 8) {  // E4M3: the hi and the lo group
+              uint32_t o[G];
+              tm_ld<G>(trow + ocol + g, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < G; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+              tm_st<G>(trow + ocol + g, o);
+            }
+            tmem_wait_st();
+#pragma unroll
+            for (int h = 0; h < G; ++h) lt[h] *= alpha[h];
+          }
         }
         float pr[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          pr[h] = mine ? ex2_approx(t[h] - mr[h]) : 0.f;
-          lt[h] += pr[h];
-        }
+        for (int h = 0; h < G; ++h) pr[h] = mine ? ex2_approx(t[h] - mr[h]) : 0.f;
+        write_p(b, jj, pr);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
+          lt[h] += pr[h];
           if (jj) {
             mref[1][h] = mr[h];
             lth[1][h] = lt[h];
@@ -896,25 +953,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mref[0][h] = mr[h];
             lth[0][h] = lt[h];
           }
-        }
-        if constexpr (F8) {
-          // P' = 256 p as E4M3 hi + lo, one byte per row of the slot
-#pragma unroll
-          for (int h = 0; h < G; h += 2) {
-            const float x0 = 256.f * pr[h], x1 = h + 1 < G ? 256.f * pr[h + 1] : 0.f;
-            const uint16_t hi = float2_to_e4m3x2(x0, x1);
-            const float2 hf = e4m3x2_to_float2(hi);
-            const uint16_t lo = float2_to_e4m3x2(x0 - hf.x, x1 - hf.y);
-            *prow8(b, 16 * jj + h) = (unsigned char)(hi & 0xffu);
-            *prow8(b, 16 * jj + 8 + h) = (unsigned char)(lo & 0xffu);
-            if (h + 1 < G) {
-              *prow8(b, 16 * jj + h + 1) = (unsigned char)(hi >> 8);
-              *prow8(b, 16 * jj + 8 + h + 1) = (unsigned char)(lo >> 8);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < G; ++h) *prow(b, jj, h) = bf16_bits(pr[h]);
         }
         dirty |= 1 << (2 * b + jj);
         if (nact == 1 && (dirty & (1 << (2 * b + (1 - jj))))) {  // the idle slot's rows to zero
