@@ -832,6 +832,97 @@ __global__ void __launch_bounds__(kThreads, 1)
     // from, so it moves only for a score 1.75 above them (P' then peaks at
     // 128 and loses one octave at the bottom, below 2^-16 of the maximum)
     constexpr float kHead = F8 ? 1.f : 0.f;
+    auto epilogue = [&](const SlotRec& e0, const SlotRec& e1, int eb, int ei, const float (&em)[2][G],
+                        const float (&el)[2][G]) -> bool {
+      if (!wait(M::B_PFREE + eb, ei / kSP)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const SlotRec rc = j == 0 ? e0 : e1;
+        if (!(rc.flags & F_LAST)) continue;
+        float ls[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) ls[h] = el[j][h];
+        if (!block_reduce(ls, false)) return false;
+        const uint32_t ocol = M::kTmO + L::kSlotCols * j;
+        float o[G];
+        {
+          uint32_t oa[G];
+          tm_ld<G>(trow + ocol, oa);
+          if constexpr (F8) {  // hi + lo groups, back from P' = 256 p
+            uint32_t ob[G];
+            tm_ld<G>(trow + ocol + 8, ob);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              o[h] = (__uint_as_float(oa[h]) + __uint_as_float(ob[h])) * (1.f / 256.f);
+          } else {
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < G; ++h) o[h] = __uint_as_float(oa[h]);
+          }
+        }
+        if (rc.flags & F_WHOLE) {
+          float mh[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) mh[h] = em[j][h];
+          // Cascade: the prefix partials of this (token, kv head), one per
+          // key chunk, folded in by log-sum-exp renormalisation.
+#pragma unroll 1
+          for (int c = 0; c < p.prefix_chunks; ++c) {
+            const float* const sl =
+                p.prefix_partials + (((size_t)c * p.num_tokens + rc.tok) * Hkv + rc.kv) * p.slot_floats;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              const float mc = __ldcg(sl + h);
+              const float mn = fmaxf(mh[h], mc);
+              const float a = exp2f(mh[h] - mn), bb = exp2f(mc - mn);
+              ls[h] = ls[h] * a + __ldcg(sl + G + h) * bb;
+              o[h] = o[h] * a + __ldcg(sl + 16 + h * kD + m) * bb;
+              mh[h] = mn;
+            }
+          }
+          uint16_t* const orow = p.out + ((size_t)rc.tok * Hq + (size_t)rc.kv * G) * kD + m;
+#pragma unroll
+          for (int h = 0; h < G; ++h) orow[h * kD] = bf16_bits(o[h] * (p.v_scale / ls[h]));
+        } else {
+          // a partial (m, l, o) for the merge pass in slot u + w: tokens
+          // increase with the position order, so the slot is unique per portion
+          float* const slot =
+              p.partials + (size_t)(rc.tok * Hkv + rc.kv + w) * (size_t)p.slot_floats;
+          if (m == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              __stcg(slot + h, em[j][h]);
+              __stcg(slot + G + h, ls[h]);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) __stcg(slot + 16 + h * kD + m, o[h]);
+        }
+        // the slot's columns start the next portion at zero
+        uint32_t z[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) z[c] = 0u;
+#pragma unroll
+        for (int g = 0; g < L::kSlotCols; g += 8) tm_st<8>(trow + ocol + g, z);
+        tmem_wait_st();
+      }
+      tc_fence_before();  // the next tile's P.V accumulates into O^T
+      return true;
+    };
+    // A tile's epilogue (portions ending there) runs while the next tile is
+    // in the softmax, before that tile's P is released to the MMA warp: by
+    // then tile i's P.V has usually completed, and the next P.V, which would
+    // accumulate into the slot's columns, waits for the epilogue's reads and
+    // zeroing. The ending slots' maxima and sums are kept for it. At G = 8
+    // (long portions, few epilogues, more registers) it runs right after the
+    // tile, once its P.V has completed (measured faster there, slower at G <= 4).
+    constexpr bool kDefer = G <= 4;
+    bool pend = false;
+    SlotRec pr0{0, 0, 0, 0, 0, 0, 0, 0}, pr1{0, 0, 0, 0, 0, 0, 0, 0};
+    int pb = 0, pi = 0;
+    float pm[2][G], pl[2][G];
     int i = 0;
     bool ok = true;
 #pragma unroll 1
@@ -989,91 +1080,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       fence_proxy_async_smem();  // generic-proxy stores -> visible to the tensor core
+      if (pend) {  // the previous tile's epilogue, before this tile's P.V may start
+        if (!epilogue(pr0, pr1, pb, pi, pm, pl)) { ok = false; break; }
+        pend = false;
+      }
       tc_fence_before();
       mbar_arrive(BAR(M::B_PREADY + b));
-
-      if ((r0.flags | r1.flags) & F_LAST) {
-        // ---- epilogue of the portions ending here: O^T complete once tile
-        // i's P.V is ----
-        if (!wait(M::B_PFREE + b, i / kSP)) { ok = false; break; }
-        tc_fence_after();
+      if (((r0.flags | r1.flags) & F_LAST) && !kDefer) {  // the epilogue now
+        if (!epilogue(r0, r1, b, i, mref, lth)) { ok = false; break; }
+      } else if ((r0.flags | r1.flags) & F_LAST) {
+        pend = true;
+        pr0 = r0;
+        pr1 = r1;
+        pb = b;
+        pi = i;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const SlotRec rc = j == 0 ? r0 : r1;
-          if (!(rc.flags & F_LAST)) continue;
-          float ls[G];
+        for (int j = 0; j < 2; ++j)
 #pragma unroll
-          for (int h = 0; h < G; ++h) ls[h] = lth[j][h];
-          if (!block_reduce(ls, false)) { ok = false; break; }
-          const uint32_t ocol = M::kTmO + L::kSlotCols * j;
-          float o[G];
-          {
-            uint32_t oa[G];
-            tm_ld<G>(trow + ocol, oa);
-            if constexpr (F8) {  // hi + lo groups, back from P' = 256 p
-              uint32_t ob[G];
-              tm_ld<G>(trow + ocol + 8, ob);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < G; ++h)
-                o[h] = (__uint_as_float(oa[h]) + __uint_as_float(ob[h])) * (1.f / 256.f);
-            } else {
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < G; ++h) o[h] = __uint_as_float(oa[h]);
-            }
+          for (int h = 0; h < G; ++h) {
+            pm[j][h] = mref[j][h];
+            pl[j][h] = lth[j][h];
           }
-          if (rc.flags & F_WHOLE) {
-            float mh[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) mh[h] = mref[j][h];
-            // Cascade: the prefix partials of this (token, kv head), one per
-            // key chunk, folded in by log-sum-exp renormalisation.
-#pragma unroll 1
-            for (int c = 0; c < p.prefix_chunks; ++c) {
-              const float* const sl =
-                  p.prefix_partials + (((size_t)c * p.num_tokens + rc.tok) * Hkv + rc.kv) * p.slot_floats;
-#pragma unroll
-              for (int h = 0; h < G; ++h) {
-                const float mc = __ldcg(sl + h);
-                const float mn = fmaxf(mh[h], mc);
-                const float a = exp2f(mh[h] - mn), bb = exp2f(mc - mn);
-                ls[h] = ls[h] * a + __ldcg(sl + G + h) * bb;
-                o[h] = o[h] * a + __ldcg(sl + 16 + h * kD + m) * bb;
-                mh[h] = mn;
-              }
-            }
-            uint16_t* const orow = p.out + ((size_t)rc.tok * Hq + (size_t)rc.kv * G) * kD + m;
-#pragma unroll
-            for (int h = 0; h < G; ++h) orow[h * kD] = bf16_bits(o[h] * (p.v_scale / ls[h]));
-          } else {
-            // a partial (m, l, o) for the merge pass in slot u + w: tokens
-            // increase with the position order, so the slot is unique per portion
-            float* const slot =
-                p.partials + (size_t)(rc.tok * Hkv + rc.kv + w) * (size_t)p.slot_floats;
-            if (m == 0) {
-#pragma unroll
-              for (int h = 0; h < G; ++h) {
-                __stcg(slot + h, mref[j][h]);
-                __stcg(slot + G + h, ls[h]);
-              }
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) __stcg(slot + 16 + h * kD + m, o[h]);
-          }
-          // the slot's columns start the next portion at zero
-          uint32_t z[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) z[c] = 0u;
-#pragma unroll
-          for (int g = 0; g < L::kSlotCols; g += 8) tm_st<8>(trow + ocol + g, z);
-          tmem_wait_st();
-        }
-        if (!ok) break;
-        tc_fence_before();  // the next tile's P.V accumulates into O^T
       }
       ++i;
     }
+    if (ok && pend) epilogue(pr0, pr1, pb, pi, pm, pl);  // the last tile's
   }
 
   tc_fence_before();
