@@ -97,16 +97,18 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "of fallback"}
 
 
-# The split-KV kernel a bf16 call routes to (the library's default routing):
-# the tensor-core kernel for groups of 4 or 8 query heads per KV head at
-# head_dim 128, the CUDA-core kernel otherwise.
+# The split-KV kernel a call routes to (the library's default routing): the
+# tensor-core kernel for groups of 4 or 8 query heads per KV head at head_dim
+# 128, over a bf16 or an E4M3 cache, except a cascade's suffix pass; the
+# CUDA-core kernel otherwise. Forced ("tensor-core"), it also takes the other
+# groups and (bf16) a cascade's suffixes.
 def split_kv_kernel(w: wl.Workload, fp8: bool = False, cascade: bool = False,
                     force: str = "auto") -> tuple:
     g = w.num_q_heads // w.num_kv_heads
-    tc_ok = w.head_dim == 128 and not fp8 and not cascade
+    tc_ok = w.head_dim == 128 and not (fp8 and cascade)
     if force == "cuda-core" or not tc_ok:
         return "pa_decode_kernel", "decode.cu"
-    if force == "tensor-core" or g >= 4:
+    if force == "tensor-core" or (g >= 4 and not cascade):
         return "pa_decode_tc_kernel", "decode_tc.cu"
     return "pa_decode_kernel", "decode.cu"
 
@@ -472,6 +474,8 @@ def fp8_timing(args, flush, torch, binding, dist, rank, world, peaks) -> dict:
             "steps": steps, "ms_per_step": round(ms, 5), "decode_kernel_ms": round(dec, 5),
             "kv_bytes": kv8, "algorithmic_bytes_per_launch": attn8,
             "achieved_gbs": round(achieved, 1), "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": ncu_traffic(wl.CONFIG_NAMES[HEADLINE_CONFIG] + "-e4m3",
+                                   split_kv_kernel(w, fp8=True, cascade=False)[1]),
             "peak_source": peaks["source"],
             "requests_per_s": round(world * w.num_reqs / (ms * 1e-3), 1)}
 
@@ -627,7 +631,7 @@ def run_ours(args, rank, world, local, dist):
             "bound": "hbm", "kernel": kname,
             "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["source"],
-            "traffic": ncu_traffic(wl.CONFIG_NAMES[args.config], ksrc),
+            "traffic": ncu_traffic(wl.CONFIG_NAMES[args.config] + ("-e4m3" if args.fp8 else ""), ksrc),
             "algorithmic_bytes_per_launch": sb["attention"],
             "kernel_ms": round(main["dec_ms"], 5)},
         "gpu_launches": int(main["t"]["launches"]),

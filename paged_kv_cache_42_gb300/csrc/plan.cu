@@ -81,15 +81,16 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
   __syncthreads();
 
   // a request is valid when its span lies in [0, T] and its lengths agree
+  // (the three loads are issued together: one DRAM round trip, not two)
   auto check = [&](int r, int& q0, int& qlen, int& L, bool report) -> bool {
-    q0 = p.qsl[r];
-    const int q1 = p.qsl[r + 1];
+    q0 = __ldg(p.qsl + r);
+    const int q1 = __ldg(p.qsl + r + 1);
+    L = __ldg(p.seq_lens + r);
     if (q0 < 0 || q1 < q0 || q1 > T) {
       if (report) report_error(p.err, PA_DEVERR_QSL, r);
       return false;
     }
     qlen = q1 - q0;
-    L = p.seq_lens[r];
     if (L < qlen || (L + kBlockSize - 1) / kBlockSize > p.max_blocks_per_req ||
         qlen > p.max_query_len || L > p.max_seq_len ||
         L - qlen < p.prefix_blocks * kBlockSize) {
