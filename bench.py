@@ -99,8 +99,9 @@ def measured_peaks() -> dict:
 
 # The split-KV kernel a call routes to (the library's default routing): the
 # tensor-core kernel for groups of 4 or 8 query heads per KV head at head_dim
-# 128, over a bf16 or an E4M3 cache, except a cascade's suffix pass; the
-# CUDA-core kernel otherwise. Forced ("tensor-core"), it also takes the other
+# 128, over a bf16 or an E4M3 cache (eight KV heads over E4M3: its
+# token-major form), except a cascade's suffix pass; the CUDA-core kernel
+# otherwise. Forced ("tensor-core"), it also takes the other
 # groups and (bf16) a cascade's suffixes.
 def split_kv_kernel(w: wl.Workload, fp8: bool = False, cascade: bool = False,
                     force: str = "auto") -> tuple:
@@ -109,6 +110,8 @@ def split_kv_kernel(w: wl.Workload, fp8: bool = False, cascade: bool = False,
     if force == "cuda-core" or not tc_ok:
         return "pa_decode_kernel", "decode.cu"
     if force == "tensor-core" or (g >= 4 and not cascade):
+        if fp8 and w.num_kv_heads == 8:  # E4M3 over eight KV heads: token-major tiles
+            return "pa_decode_tm_kernel", "decode_tm.cu"
         return "pa_decode_tc_kernel", "decode_tc.cu"
     return "pa_decode_kernel", "decode.cu"
 

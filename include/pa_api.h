@@ -364,6 +364,15 @@ pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event
 #define PA_OPT_DECODE_TC 2
 #define PA_OPT_DECODE_MAX_WORKERS 3
 #define PA_OPT_MIXED_OVERLAP 4
+/*
+ *   PA_OPT_DECODE_TOKEN_MAJOR (default 1): over an E4M3 cache with eight KV
+ *     heads at head_dim 128, the tensor-core split-KV kernel takes one 16-key
+ *     block of all eight KV heads per tile (one tensor copy each for K and V,
+ *     each head's keys in one half-warp). 0: the per-(token, kv head) tiles
+ *     of the other groupings. Both are within the attention tolerances of
+ *     the exact result on the same codes; they are not bit-identical.
+ */
+#define PA_OPT_DECODE_TOKEN_MAJOR 5
 pa_status pa_set_option(int option, int value);
 
 /* Number of kernel launches the library has issued in this process. */

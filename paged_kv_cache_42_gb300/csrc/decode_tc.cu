@@ -196,67 +196,6 @@ struct Rec {
 };
 static_assert(sizeof(Rec) == 64, "records are 64 bytes");
 
-// Instruction descriptor with fp32 D: kind::f16 with bf16 A/B, or (f8)
-// kind::f8f6f4 with E4M3 A/B (format code 0); a_mn / b_mn select the
-// M/N-major (transposed) form of each operand.
-constexpr uint32_t idesc_tc(int M, int N, bool a_mn, bool b_mn, bool f8 = false) {
-  return (1u << 4) | (f8 ? 0u : ((1u << 7) | (1u << 10))) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem desc] * B[smem desc], E4M3 inputs, fp32 accumulate.
-__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-
-// TMEM loads/stores of N consecutive 32-bit columns of the warp's 32 lanes.
-template <int N>
-__device__ __forceinline__ void tm_ld(uint32_t taddr, uint32_t (&r)[N]) {
-  if constexpr (N == 1) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr) : "memory");
-  } else if constexpr (N == 2) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
-                 : "=r"(r[0]), "=r"(r[1]) : "r"(taddr) : "memory");
-  } else if constexpr (N == 4) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr) : "memory");
-  } else {
-    static_assert(N == 8, "1, 2, 4 or 8 columns");
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                   "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr)
-                 : "memory");
-  }
-}
-template <int N>
-__device__ __forceinline__ void tm_st(uint32_t taddr, const uint32_t (&r)[N]) {
-  if constexpr (N == 1) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r[0]) : "memory");
-  } else if constexpr (N == 2) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(r[0]),
-                 "r"(r[1])
-                 : "memory");
-  } else if constexpr (N == 4) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-                 : "memory");
-  } else {
-    static_assert(N == 8, "1, 2, 4 or 8 columns");
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                     taddr),
-                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-  }
-}
-
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }

@@ -33,21 +33,27 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
   __shared__ float s_m[kMergeWarps][G], s_l[kMergeWarps][G];
   __shared__ __align__(16) float s_o[kMergeWarps][G][D];
   griddep_wait();  // the split-KV grid's partials and tasks
-  const int w = blockIdx.x + 1;
+  // token-major split-KV: one task per boundary for all kv heads, a CTA each
+  const int w = (p.token_major ? (int)blockIdx.x / p.num_kv_heads : (int)blockIdx.x) + 1;
   const int W = __ldcg(&p.header->num_positions);
   const int4 task = __ldcg(p.tasks + w);
   // tasks past this call's worker count are stale
   int nw = p.num_workers;
   if (p.workers_from_header) nw = min(nw, __ldcg(&p.header->decode_workers));
   if (W <= 0 || w >= plan_workers(W, nw) || task.x < 0) return;
-  const int tok = task.x, kv = task.y, wf = task.z, wl = task.w;
+  const int tok = task.x, wf = task.z, wl = task.w;
+  const int kv = p.token_major ? (int)blockIdx.x % p.num_kv_heads : task.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   // The partials: the suffix slots wf .. wl, then (cascade) the prefix chunks.
+  // Worker wf + i's slot: u + wf + i (u = token * Hkv + kv head), or
+  // token-major (token + wf + i) * Hkv + kv head.
   const int u = tok * p.num_kv_heads + kv;
   const int ns = wl - wf + 1, n = ns + p.prefix_chunks;
   auto slot = [&](int i) -> const float* {
-    return i < ns ? p.partials + (size_t)(u + wf + i) * p.slot_floats
+    const size_t s0 = p.token_major ? (size_t)(tok + wf + i) * p.num_kv_heads + kv
+                                    : (size_t)(u + wf + i);
+    return i < ns ? p.partials + s0 * p.slot_floats
                   : p.prefix_partials +
                         (((size_t)(i - ns) * p.num_tokens + tok) * p.num_kv_heads + kv) *
                             p.slot_floats;
@@ -122,10 +128,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
 
 template <int D, int G>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
-  const int boundaries = p.num_workers - 1;
+  const int boundaries = (p.num_workers - 1) * (p.token_major ? p.num_kv_heads : 1);
   if (boundaries <= 0) return cudaSuccess;  // one worker: nothing is ever split
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)boundaries);  // one CTA per slice boundary
+  cfg.gridDim = dim3((unsigned)boundaries);  // one CTA per slice boundary (and kv head)
   cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;

@@ -41,6 +41,7 @@ std::atomic<int> g_self_plan{1};  // pa_set_option(PA_OPT_DECODE_SELF_PLAN, ...)
 std::atomic<int> g_decode_tc{1};  // pa_set_option(PA_OPT_DECODE_TC, ...): 0 off, 1 auto, 2 on
 std::atomic<int> g_max_workers{0};  // pa_set_option(PA_OPT_DECODE_MAX_WORKERS, ...): 0 = no cap
 std::atomic<int> g_mixed_overlap{1};  // pa_set_option(PA_OPT_MIXED_OVERLAP, ...)
+std::atomic<int> g_token_major{1};  // pa_set_option(PA_OPT_DECODE_TOKEN_MAJOR, ...)
 constexpr int kNumTimers = 6;  // write, plan, decode, prefill, cascade prefix, merge
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
@@ -322,6 +323,11 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   if (launched <= 0) return PA_ERR_CUDA;
   const int cap = g_max_workers.load();
   pp.num_workers = (cap > 0 && cap < launched) ? cap : launched;
+  // An E4M3 cache over eight KV heads takes the token-major tiles (one block
+  // of every KV head per tile) on the tensor cores.
+  const bool use_tm = use_tc && kv_fp8 && g_token_major.load() &&
+                      decode_tm_supported(head_dim, group, num_kv_heads, launched);
+  pp.token_major = use_tm ? 1 : 0;
   // A mixed batch on the tensor-core split-KV kernel (bf16) may run its
   // prefill chunks on a few SMs beside the split-KV work (the planner decides
   // how many, or none); the E4M3 path keeps its query-split pass between them.
@@ -419,9 +425,10 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   {
     TimerScope timer(2, s);
     const cudaError_t e =
-        use_tc ? launch_decode_tc(dp, group, kv_fp8 != 0, d->num_sms, s, &launched_workers)
-               : launch_decode(dp, head_dim, group, kv_fp8 != 0, d->num_sms, occ_cap, s,
-                               &launched_workers);
+        use_tm   ? launch_decode_tm(dp, group, d->num_sms, s, &launched_workers)
+        : use_tc ? launch_decode_tc(dp, group, kv_fp8 != 0, d->num_sms, s, &launched_workers)
+                 : launch_decode(dp, head_dim, group, kv_fp8 != 0, d->num_sms, occ_cap, s,
+                                 &launched_workers);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
   }
@@ -435,6 +442,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   mp.slot_floats = lay.slot_floats;
   mp.num_workers = workers;
   mp.workers_from_header = overlap;
+  mp.token_major = pp.token_major;
   mp.num_q_heads = num_q_heads;
   mp.num_kv_heads = num_kv_heads;
   mp.num_tokens = num_tokens;
@@ -537,6 +545,9 @@ pa_status pa_set_option(int option, int value) {
     case PA_OPT_DECODE_TC:
       if (value < 0 || value > 2) return PA_ERR_INVALID_ARG;
       g_decode_tc.store(value);
+      return PA_OK;
+    case PA_OPT_DECODE_TOKEN_MAJOR:
+      g_token_major.store(value ? 1 : 0);
       return PA_OK;
     case PA_OPT_MIXED_OVERLAP:
       g_mixed_overlap.store(value ? 1 : 0);

@@ -176,6 +176,7 @@ struct PlanParams {
   // prefill-chunk and split-KV grids (num_sms of them; position_bytes of
   // K and V per split-KV position)
   int overlap, num_sms, position_bytes;
+  int token_major;  // positions per token are its blocks (all kv heads at once)
   WsHeader* header;
   UnitInfo* units;
   PrefillTile* tiles;
@@ -266,6 +267,9 @@ struct MergeParams {
   int slot_floats;
   int num_workers;  // split-KV workers launched (the slicing's upper bound)
   int workers_from_header;  // overlapped mixed batch: header->decode_workers, if fewer
+  int token_major;          // token-major split-KV: a task {token, -, wf, wl} covers every
+                            // kv head (CTA blockIdx = boundary * Hkv + kv head), slot
+                            // (token + w) * Hkv + kv head
   int num_q_heads, num_kv_heads, num_tokens;
   int key_start_blocks;
   const float* prefix_partials;
@@ -321,8 +325,9 @@ cudaError_t launch_merge(const MergeParams& p, int head_dim, int group, cudaStre
 int decode_workers(int head_dim, int group, bool f8, int num_sms, int occ_cap);
 
 // Tensor-core split-KV decode (decode_tc.cu): one CTA per SM is one worker.
-// Supported for head_dim 128 over a bf16 cache without a cascade prefix; it
-// takes the same plan, partial slots and merge tasks as launch_decode.
+// Supported for head_dim 128, over a bf16 cache (a cascade's suffix pass
+// included) or an E4M3 cache; it takes the same plan, partial slots and merge
+// tasks as launch_decode.
 bool decode_tc_supported(int head_dim, int group, bool f8, int key_start_blocks);
 int decode_tc_workers(int num_sms);
 cudaError_t launch_decode_tc(const DecodeParams& p, int group, bool f8, int num_sms,
@@ -331,6 +336,13 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int group, bool f8, int num_
 // p.qsplit / p.qinv), as a programmatic dependent of the preceding grid that
 // completes only after it.
 cudaError_t launch_qsplit(const DecodeParams& p, int group, cudaStream_t s);
+// Token-major tensor-core split-KV decode over an E4M3 cache (decode_tm.cu):
+// eight KV heads, head_dim 128. Its positions are (token, block) - the plan
+// built with PlanParams::token_major - and its partial of (token, kv head)
+// from worker w sits in slot (token + w) * 8 + kv head (MergeParams::token_major).
+bool decode_tm_supported(int head_dim, int group, int num_kv_heads, int workers);
+cudaError_t launch_decode_tm(const DecodeParams& p, int group, int num_sms, cudaStream_t s,
+                             int* workers_out);
 
 // 2-D tiled tensor map (CUtensorMap, passed as void*) over a row-major bf16
 // matrix of `rows` rows of `inner` elements, `row_stride_bytes` apart, with a

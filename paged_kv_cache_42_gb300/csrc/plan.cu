@@ -176,7 +176,9 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
     const int2 u = t < T ? raw[t] : make_int2(-1, 0);
     // blocks on the split-KV path: all the token sees, less a cascade prefix
     const int nb = max(0, (u.y + kBlockSize - 1) / kBlockSize - p.prefix_blocks);
-    const long long packed = ((long long)(nb > 0) << 40) | ((long long)nb * p.num_kv_heads);
+    // (token-major split-KV: one position per block, every kv head at once)
+    const long long packed =
+        ((long long)(nb > 0) << 40) | ((long long)nb * (p.token_major ? 1 : p.num_kv_heads));
     long long total;
     const long long ex = block_exclusive_scan(packed, &total, scan_sm);  // syncs: raw reads done
     if (nb > 0) {

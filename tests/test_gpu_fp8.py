@@ -166,16 +166,20 @@ def decode_tc_option():
     yield binding.set_option
     binding.set_option("decode_tc", 1)
     binding.set_option("decode_max_workers", 0)
+    binding.set_option("decode_token_major", 1)
 
 
 @pytest.mark.parametrize("i", range(len(TC_CASES)))
-@pytest.mark.parametrize("tc", [0, 2])
-def test_attention_fp8_both_split_kv_kernels(i, tc, decode_tc_option):
+@pytest.mark.parametrize("tc,tm", [(0, 1), (2, 1), (2, 0)])
+def test_attention_fp8_both_split_kv_kernels(i, tc, tm, decode_tc_option):
+    # tc 2 with eight KV heads: the token-major tiles (tm 1) or the
+    # per-(token, kv head) tiles (tm 0)
     ctx, ql, hq, hkv = TC_CASES[i]
     w = wl.make_workload(ctx, ql, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
                          seed=1160 + i, pool_factor=1.3)
     decode_tc_option("decode_tc", tc)
-    run(w, 0.0113, 0.0127, f"fp8 split-KV kernel {tc} case {i}")
+    decode_tc_option("decode_token_major", tm)
+    run(w, 0.0113, 0.0127, f"fp8 split-KV kernel {tc}/{tm} case {i}")
 
 
 def test_attention_fp8_tensor_core_running_max_and_splits(decode_tc_option):
@@ -192,6 +196,58 @@ def test_attention_fp8_tensor_core_running_max_and_splits(decode_tc_option):
     run(w, 0.03, 1.0, "fp8 tc running max")
     decode_tc_option("decode_max_workers", 5)
     run(w, 0.03, 1.0, "fp8 tc running max, 5 parts")
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_token_major_running_max_and_splits(g, decode_tc_option):
+    # Eight KV heads whose scores grow along the sequence at head-dependent
+    # rates: references move in some half-warps and not others (O^T columns
+    # rescaled per query head); then the same over 1, 2 and 7 workers (token
+    # partials per kv head in slots (token + worker) * 8 + kv head)
+    L0 = 1500
+    w = wl.make_workload([L0 - 1, 300], [1, 1], num_q_heads=8 * g, num_kv_heads=8,
+                         head_dim=128, seed=1180 + g)
+    w.q[...] = wl.to_bf16_bits(np.float32(1.0))
+    for kv in range(8):
+        rate = 0.01 * kv
+        for p in range(L0 - 1):
+            w.k_cache[w.block_tables[0, p // 16], kv, p % 16, :] = wl.to_bf16_bits(
+                np.float32(rate * (p // 64)))
+        w.k_new[0, kv] = wl.to_bf16_bits(np.float32(rate * ((L0 - 1) // 64)))
+    decode_tc_option("decode_tc", 2)
+    run(w, 0.03, 1.0, f"fp8 token-major running max, G {g}")
+    for n in (1, 2, 7):
+        decode_tc_option("decode_max_workers", n)
+        run(w, 0.03, 1.0, f"fp8 token-major running max, G {g}, {n} parts")
+
+
+def test_token_major_random_batches(decode_tc_option):
+    # decode-only batches (self-planned) and batches with short spans and
+    # tensor-core chunks (planner path), at every group size
+    rng = np.random.default_rng(1190)
+    for it in range(6):
+        R = int(rng.integers(1, 50))
+        ctx = rng.integers(0, 3000, size=R)
+        ql = np.ones(R, np.int64) if it % 2 == 0 else np.where(
+            rng.random(R) < 0.8, 1, rng.integers(0, 40, size=R))
+        ctx = np.maximum(ctx, np.where(ql == 0, 1, 0))
+        g = [1, 2, 4, 8][it % 4]
+        w = wl.make_workload(ctx, ql, num_q_heads=8 * g, num_kv_heads=8, head_dim=128,
+                             seed=1191 + it, pool_factor=1.2)
+        run(w, 0.0113, 0.0127, f"fp8 token-major random batch {it}")
+
+
+def test_token_major_against_per_head_tiles(decode_tc_option):
+    # the two tile shapes agree within the tolerance on the Llama-8B batch
+    w = wl.make_config(2)
+    b = Fp8Batch(w, 0.0113, 0.0127)
+    b.write()
+    a = gu.to_f64(b.attend())
+    decode_tc_option("decode_token_major", 0)
+    c = gu.to_f64(b.attend())
+    torch.cuda.synchronize()
+    gu.check_no_device_error()
+    assert np.abs(a - c).max() <= gu.MAX_ABS
 
 
 def test_attention_fp8_extreme_query_rows(decode_tc_option):
