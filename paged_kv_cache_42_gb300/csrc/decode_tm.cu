@@ -301,20 +301,29 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         p.merge_tasks[w] = task;
       }
     }
-    // the split query rows and scales (and the K/V write before them) come
-    // from the preceding grids
-    if (p.self_plan) griddep_wait();
+    // The split query rows and scales, and the K/V write before them, come
+    // from the preceding grids: a planned batch waited for them at the top; a
+    // self-planned one waits below, after the K/V copies of its first two
+    // tiles that the write does not touch.
+    bool waited = !p.self_plan;
 
     struct Meta {
       TmRec r;
       int live;      // 0: no more tiles
+      int lastblk;   // the token's last block (it holds the newest key)
       int pid;       // lane 0: the block id (loaded two tiles ahead of its copy)
       float inv0, inv1;  // lanes: 2^-e of query rows lane and lane + 32
+    };
+    auto load_inv = [&](Meta& t) {  // query row kv * G + g's scale: qinv[(token * 8 + kv) * 8 + g]
+      const size_t qb = (size_t)t.r.tok * kTmHkv * 8;
+      if (lane < HQ) t.inv0 = __ldg(p.qinv + qb + (lane / G) * 8 + (lane % G));
+      if (lane + 32 < HQ) t.inv1 = __ldg(p.qinv + qb + ((lane + 32) / G) * 8 + ((lane + 32) % G));
     };
     auto next_tile = [&]() -> Meta {
       Meta t;
       t.r = TmRec{0, 0, 0, T_END, {0, 0, 0, 0}};
       t.live = 0;
+      t.lastblk = 0;
       t.pid = 0;
       t.inv0 = t.inv1 = 0.f;
       if (y >= E) return t;
@@ -325,11 +334,9 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                       ((np & 1) ? T_PAR : 0),
                   {0, 0, 0, 0}};
       t.live = 1;
+      t.lastblk = blk + 1 == nb;
       if (lane == 0) t.pid = __ldg(p.block_tables + (size_t)U.req * p.bt_stride + blk);
-      // query row kv * G + g's scale sits at qinv[(token * 8 + kv) * 8 + g]
-      const size_t qb = (size_t)U.tok * kTmHkv * 8;
-      if (lane < HQ) t.inv0 = __ldg(p.qinv + qb + (lane / G) * 8 + (lane % G));
-      if (lane + 32 < HQ) t.inv1 = __ldg(p.qinv + qb + ((lane + 32) / G) * 8 + ((lane + 32) % G));
+      if (waited) load_inv(t);
       pfirst = false;
       ++y;
       ++blk;
@@ -352,6 +359,15 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     int* const qtag = reinterpret_cast<int*>(gb + L::OFF_QTAG);
     if (lane < kStages) qtag[lane] = -1;
     __syncwarp();
+    auto block_id = [&](const Meta& t) -> int {
+      int pid = t.pid;
+      if (pid < 0 || pid >= p.num_blocks) {
+        report_error(p.err, PA_DEVERR_BLOCK_ID, t.r.key0 / kBlockSize);
+        pid = 0;
+      }
+      return pid;
+    };
+    bool pre0 = false, pre1 = false;  // tiles 0 and 1: K/V copies already issued
     auto issue = [&](const Meta& cur, Meta& nxt2) -> bool {  // false: stop
       nxt2 = next_tile();
       const int st = i % kStages;
@@ -373,15 +389,15 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       if (lane == 0) {
         recs[st] = cur.r;
         if (needq) qtag[st] = cur.r.tok;
-        mbar_arrive_expect_tx(full, 2u * L::kKvTile + (needq ? (uint32_t)L::kQBytes : 0u));
-        int pid = cur.pid;
-        if (pid < 0 || pid >= p.num_blocks) {
-          report_error(p.err, PA_DEVERR_BLOCK_ID, cur.r.key0 / kBlockSize);
-          pid = 0;
-        }
+        const bool kv_done = (i == 0 && pre0) || (i == 1 && pre1);
+        mbar_arrive_expect_tx(full, (kv_done ? 0u : 2u * L::kKvTile) +
+                                        (needq ? (uint32_t)L::kQBytes : 0u));
         const uint32_t sbase = base + L::OFF_STAGE + st * L::kStageBytes;
-        tma_load_2d(sbase, &tp.tm_k, 0, pid * kTmHkv * kBlockSize, full);
-        tma_load_2d(sbase + L::kKvTile, &tp.tm_v, 0, pid * kTmHkv * kBlockSize, full);
+        if (!kv_done) {
+          const int pid = block_id(cur);
+          tma_load_2d(sbase, &tp.tm_k, 0, pid * kTmHkv * kBlockSize, full);
+          tma_load_2d(sbase + L::kKvTile, &tp.tm_v, 0, pid * kTmHkv * kBlockSize, full);
+        }
         if (needq) tma_load_3d(sbase + 2 * L::kKvTile, &tp.tm_q, 0, cur.r.tok * HQ, 0, full);
       }
       __syncwarp();
@@ -390,6 +406,28 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     };
     Meta ma = next_tile();
     Meta mb = next_tile();
+    if (!waited) {
+      // the first two tiles' K and V (stages 0 and 1), unless they hold a
+      // token's newest key
+      auto pre_issue = [&](const Meta& t, int j) -> bool {
+        if (!t.live || t.lastblk) return false;
+        if (lane == 0) {
+          const uint32_t full = BAR(L::B_FULL + j);
+          const uint32_t sbase = base + L::OFF_STAGE + j * L::kStageBytes;
+          const int pid = block_id(t);
+          mbar_expect_tx(full, 2u * L::kKvTile);
+          tma_load_2d(sbase, &tp.tm_k, 0, pid * kTmHkv * kBlockSize, full);
+          tma_load_2d(sbase + L::kKvTile, &tp.tm_v, 0, pid * kTmHkv * kBlockSize, full);
+        }
+        return true;
+      };
+      pre0 = pre_issue(ma, 0);
+      pre1 = pre_issue(mb, 1);
+      griddep_wait();
+      waited = true;
+      if (ma.live) load_inv(ma);
+      if (mb.live) load_inv(mb);
+    }
     Meta mc;
 #pragma unroll 1
     while (issue(ma, mc) && issue(mb, ma) && issue(mc, mb)) {

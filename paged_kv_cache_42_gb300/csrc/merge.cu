@@ -24,7 +24,7 @@ namespace pa {
 
 namespace {
 
-constexpr int kMergeWarps = 4;
+constexpr int kMergeWarps = 8;
 
 template <int D, int G>
 __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeParams p) {
