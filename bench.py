@@ -408,14 +408,16 @@ def time_steps(res: Resident, steps: int, warmup: int, flush, torch, binding, di
 
 def time_kernels(res: Resident, steps: int, warmup: int, flush, torch, binding, dist) -> dict:
     """Kernel durations (decode / tensor-core) from a separate timed pass.
-    The events around each launch serialise the grids, so a mixed batch is
-    timed here with the prefill / split-KV overlap off: every kernel on the
-    whole GPU, one after the other."""
+    The events around each launch serialise the grids, so a mixed batch and a
+    cascade are timed here with their overlaps off: every kernel on the whole
+    GPU, one after the other."""
     binding.set_option("mixed_overlap", 0)
+    binding.set_option("cascade_overlap", 0)
     try:
         t = time_steps(res, steps, warmup, flush, torch, binding, dist, timers=True)
     finally:
         binding.set_option("mixed_overlap", 1)
+        binding.set_option("cascade_overlap", 1)
     return {"decode_ms": max_over_ranks(t["decode_ms"], dist),
             "prefill_ms": max_over_ranks(t["prefill_ms"], dist)}
 
@@ -434,6 +436,12 @@ def prefix_share_timing(args, flush, torch, binding, dist, rank, world) -> dict:
         res = Resident(w, torch, binding, cascade_len=casc)
         t = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
         tk = time_kernels(res, steps, args.warmup, flush, torch, binding, dist)
+        if casc:  # the same step with the prefix pass first, on every SM
+            binding.set_option("cascade_overlap", 0)
+            try:
+                ts = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
+            finally:
+                binding.set_option("cascade_overlap", 1)
         code, detail = binding.get_device_error(clear=True)
         if code:
             raise RuntimeError(f"device error {code} at {detail}")
@@ -448,6 +456,10 @@ def prefix_share_timing(args, flush, torch, binding, dist, rank, world) -> dict:
         if casc:
             out[name]["prefix_kernel_ms"] = round(pre, 5)
             out[name]["common_prefix_len"] = casc
+            out[name]["serial_ms_per_step"] = round(max_over_ranks(ts["ms_per_step"], dist), 5)
+            out[name]["overlap"] = ("prefix pass on a few SMs beside the suffix pass; "
+                                    "serial_ms_per_step: the prefix pass first; kernel times "
+                                    "from a pass with the overlap off")
         del res
         torch.cuda.empty_cache()
     out["cascade_speedup"] = round(out["plain"]["ms_per_step"] / out["cascade"]["ms_per_step"], 3)

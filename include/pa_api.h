@@ -373,6 +373,16 @@ pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event
  *     the exact result on the same codes; they are not bit-identical.
  */
 #define PA_OPT_DECODE_TOKEN_MAJOR 5
+/*
+ *   PA_OPT_CASCADE_OVERLAP (default 1): in pa_attention_cascade, with the
+ *     suffix pass on the CUDA-core split-KV kernel (the default routing), the
+ *     prefix pass takes a few SMs (about two of its work items each) and the
+ *     suffix pass the rest, both at once; every (token, kv head) then leaves
+ *     fp32 partials and the merge pass folds suffix and prefix together.
+ *     Results stay within the attention tolerances (the folding order
+ *     differs). value 0: the prefix pass first, folded by the suffix pass.
+ */
+#define PA_OPT_CASCADE_OVERLAP 6
 pa_status pa_set_option(int option, int value);
 
 /* Number of kernel launches the library has issued in this process. */

@@ -141,7 +141,7 @@ struct Loc {
 };
 
 template <int D, int G, int WARPS, int NSTAGE, bool F8>
-__global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParams p) {
+__device__ __forceinline__ void decode_body(const DecodeParams& p) {
   using C = Cfg<D, G, F8>;
   using WS = WarpSmem<D, G, NSTAGE, F8>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -213,6 +213,13 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     units = su;
     W = carry;
     K = R;
+  } else if (p.overlap) {
+    // started by the cascade prefix pass once the planner (and the KV write
+    // before it) had completed: the plan is read from L2, and the prefix
+    // pass is waited for only at the end (see pa_decode_kernel)
+    waited = true;
+    W = __ldcg(&p.header->num_positions);
+    K = __ldcg(&p.header->num_units);
   } else {
     griddep_wait();  // the plan is written by the preceding grid
     waited = true;
@@ -232,9 +239,14 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
 
 
   // ---- batch metadata helpers ------------------------------------------------
+  // the planner's table (global memory, an earlier grid's) is read from L2
+  auto unit_at = [&](int k) -> int4 {
+    return p.self_plan ? *reinterpret_cast<const int4*>(units + k)
+                       : __ldcg(reinterpret_cast<const int4*>(units + k));
+  };
   auto window = [&](int kbase) -> int {
     const int kk = kbase + lane;
-    return kk <= K ? units[kk].base : 0x7fffffff;
+    return kk <= K ? unit_at(kk).w : 0x7fffffff;
   };
   auto locate = [&](int y0, int kbase, int win) -> Loc {
     const int y = y0 + lane;
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
     for (int i = 0; i < 32; ++i) c += (__shfl_sync(kFull, win, i) <= y) ? 1 : 0;
     int k = kbase + c - 1;
     k = k < 0 ? 0 : (k > K ? K : k);
-    const int4 u = *reinterpret_cast<const int4*>(units + k);
+    const int4 u = unit_at(k);
     return Loc{k, u.x, u.y, u.z, u.w};
   };
   auto finish = [&](int y0, const Loc& kl) -> Batch {
@@ -276,14 +288,14 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
   // search over units[].base --------------------------------------------------------
   int lo = 0, hi = K;  // base[lo] <= S < base[hi]
   if (p.worker_unit && !p.self_plan) {
-    lo = __ldg(p.worker_unit + w);
+    lo = __ldcg(p.worker_unit + w);
     hi = lo + 1;
   }
 #pragma unroll 1
   while (hi - lo > 1) {
     const int step = (hi - lo + 31) / 32;
     const int idx = lo + lane * step;
-    const bool ok = idx < hi && units[idx].base <= S;
+    const bool ok = idx < hi && unit_at(idx).w <= S;
     const unsigned bal = __ballot_sync(kFull, ok);
     const int last = 31 - __clz(bal);
     lo = lo + last * step;
@@ -683,7 +695,7 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
           }
         }
       };
-      if (wf == wl) {
+      if (wf == wl && !p.fold_later) {
         if (p.prefix_partials) {
           float M[G], Ls[G], O[G][C::VD];
 #pragma unroll
@@ -738,6 +750,14 @@ __global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParam
       }
     }
   }
+}
+
+template <int D, int G, int WARPS, int NSTAGE, bool F8>
+__global__ void __launch_bounds__(WARPS * 32) pa_decode_kernel(const DecodeParams p) {
+  decode_body<D, G, WARPS, NSTAGE, F8>(p);
+  // overlapped cascade: complete only after the prefix pass's grid, so that
+  // the merge pass after this grid sees the prefix partials too
+  if (p.overlap && threadIdx.x == 0) griddep_wait();
 }
 
 // ---- launch ---------------------------------------------------------------------------

@@ -33,16 +33,34 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
   __shared__ float s_m[kMergeWarps][G], s_l[kMergeWarps][G];
   __shared__ __align__(16) float s_o[kMergeWarps][G][D];
   griddep_wait();  // the split-KV grid's partials and tasks
-  // token-major split-KV: one task per boundary for all kv heads, a CTA each
-  const int w = (p.token_major ? (int)blockIdx.x / p.num_kv_heads : (int)blockIdx.x) + 1;
   const int W = __ldcg(&p.header->num_positions);
-  const int4 task = __ldcg(p.tasks + w);
-  // tasks past this call's worker count are stale
   int nw = p.num_workers;
   if (p.workers_from_header) nw = min(nw, __ldcg(&p.header->decode_workers));
-  if (W <= 0 || w >= plan_workers(W, nw) || task.x < 0) return;
-  const int tok = task.x, wf = task.z, wl = task.w;
-  const int kv = p.token_major ? (int)blockIdx.x % p.num_kv_heads : task.y;
+  if (W <= 0) return;
+  int tok, kv, wf, wl;
+  if (p.all_units) {
+    // overlapped cascade: (unit, kv head) blockIdx; its positions, and the
+    // workers holding them, as the split-KV kernel sliced them
+    const int k = (int)blockIdx.x / p.num_kv_heads;
+    kv = (int)blockIdx.x % p.num_kv_heads;
+    if (k >= __ldcg(&p.header->num_units)) return;
+    const int4 u = __ldcg(reinterpret_cast<const int4*>(p.units + k));
+    const int nb = max(1, (u.z + kBlockSize - 1) / kBlockSize - p.key_start_blocks);
+    const int first = u.w + kv * nb, NW = plan_workers(W, nw);
+    tok = u.x;
+    wf = worker_of(first, W, NW);
+    wl = worker_of(first + nb - 1, W, NW);
+  } else {
+    // token-major split-KV: one task per boundary for all kv heads, a CTA each
+    const int w = (p.token_major ? (int)blockIdx.x / p.num_kv_heads : (int)blockIdx.x) + 1;
+    const int4 task = __ldcg(p.tasks + w);
+    // tasks past this call's worker count are stale
+    if (w >= plan_workers(W, nw) || task.x < 0) return;
+    tok = task.x;
+    wf = task.z;
+    wl = task.w;
+    kv = p.token_major ? (int)blockIdx.x % p.num_kv_heads : task.y;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   // The partials: the suffix slots wf .. wl, then (cascade) the prefix chunks.
@@ -128,7 +146,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
 
 template <int D, int G>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
-  const int boundaries = (p.num_workers - 1) * (p.token_major ? p.num_kv_heads : 1);
+  // one CTA per slice boundary (and kv head), or per (token, kv head)
+  const int boundaries = p.all_units ? p.num_tokens * p.num_kv_heads
+                                     : (p.num_workers - 1) * (p.token_major ? p.num_kv_heads : 1);
   if (boundaries <= 0) return cudaSuccess;  // one worker: nothing is ever split
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)boundaries);  // one CTA per slice boundary (and kv head)

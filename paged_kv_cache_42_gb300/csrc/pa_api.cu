@@ -42,6 +42,7 @@ std::atomic<int> g_decode_tc{1};  // pa_set_option(PA_OPT_DECODE_TC, ...): 0 off
 std::atomic<int> g_max_workers{0};  // pa_set_option(PA_OPT_DECODE_MAX_WORKERS, ...): 0 = no cap
 std::atomic<int> g_mixed_overlap{1};  // pa_set_option(PA_OPT_MIXED_OVERLAP, ...)
 std::atomic<int> g_token_major{1};  // pa_set_option(PA_OPT_DECODE_TOKEN_MAJOR, ...)
+std::atomic<int> g_cascade_overlap{1};  // pa_set_option(PA_OPT_CASCADE_OVERLAP, ...)
 constexpr int kNumTimers = 6;  // write, plan, decode, prefill, cascade prefix, merge
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
@@ -318,8 +319,20 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   const bool use_tc = tc_mode != 0 &&
                       decode_tc_supported(head_dim, group, kv_fp8 != 0, prefix_len / kBlockSize) &&
                       (tc_mode == 2 || (group >= PA_DECODE_TC_MIN_GROUP && prefix_len == 0));
+  // A cascade on the CUDA-core suffix pass may run its prefix pass on a few
+  // SMs (about two prefix items each) beside the suffix pass on the rest; the
+  // merge pass then folds every (token, kv head).
+  const int c_overlap = (g_cascade_overlap.load() && prefix_len > 0 && !use_tc) ? 1 : 0;
+  int prefix_ctas = 0;
+  if (c_overlap) {
+    const int items = prefix_pairs(num_tokens, group) * num_kv_heads * chunks;
+    prefix_ctas = (items + 1) / 2;
+    if (prefix_ctas > d->num_sms / 4) prefix_ctas = d->num_sms / 4;
+    if (prefix_ctas < 1) prefix_ctas = 1;
+  }
+  const int dec_sms = d->num_sms - prefix_ctas;  // SMs the split-KV grid fills
   const int launched = use_tc ? decode_tc_workers(d->num_sms)
-                              : decode_workers(head_dim, pp.group, kv_fp8 != 0, d->num_sms, occ_cap);
+                              : decode_workers(head_dim, pp.group, kv_fp8 != 0, dec_sms, occ_cap);
   if (launched <= 0) return PA_ERR_CUDA;
   const int cap = g_max_workers.load();
   pp.num_workers = (cap > 0 && cap < launched) ? cap : launched;
@@ -372,7 +385,8 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
     pl.num_blocks = num_blocks;
     pl.bt_stride = max_blocks_per_req;
     pl.scale_log2 = scale * 1.4426950408889634f * (kv_fp8 ? k_scale : 1.f);
-    pl.overlap = overlap;
+    pl.overlap = prefix_len > 0 ? c_overlap : overlap;
+    pl.prefix_ctas = prefix_ctas;
     pl.err = d->err;
     TimerScope timer(prefix_len > 0 ? 4 : 3, s);
     const cudaError_t e = launch_prefill(pl, d->num_sms, s);
@@ -414,7 +428,8 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   dp.max_workers = cap > 0 ? cap : kMaxDecodeWorkers;
   dp.qsplit = ws + lay.qsplit_off;
   dp.qinv = reinterpret_cast<const float*>(ws + lay.qinv_off);
-  dp.overlap = overlap;
+  dp.overlap = (overlap || c_overlap) ? 1 : 0;
+  dp.fold_later = c_overlap;
   dp.err = d->err;
   if (use_tc && kv_fp8) {  // the E4M3 tensor-core kernel takes the queries split
     const cudaError_t e = launch_qsplit(dp, group, s);
@@ -427,7 +442,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
     const cudaError_t e =
         use_tm   ? launch_decode_tm(dp, group, d->num_sms, s, &launched_workers)
         : use_tc ? launch_decode_tc(dp, group, kv_fp8 != 0, d->num_sms, s, &launched_workers)
-                 : launch_decode(dp, head_dim, group, kv_fp8 != 0, d->num_sms, occ_cap, s,
+                 : launch_decode(dp, head_dim, group, kv_fp8 != 0, dec_sms, occ_cap, s,
                                  &launched_workers);
     g_launches.fetch_add(1);
     if (e != cudaSuccess) return PA_ERR_CUDA;
@@ -451,7 +466,9 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   mp.prefix_chunks = chunks;
   mp.v_scale = dp.v_scale;
   mp.out = dp.out;
-  if (workers > 1) {
+  mp.all_units = c_overlap;
+  mp.units = pp.units;
+  if (workers > 1 || c_overlap) {
     TimerScope timer(5, s);
     const cudaError_t e = launch_merge(mp, head_dim, group, s);
     g_launches.fetch_add(1);
@@ -545,6 +562,9 @@ pa_status pa_set_option(int option, int value) {
     case PA_OPT_DECODE_TC:
       if (value < 0 || value > 2) return PA_ERR_INVALID_ARG;
       g_decode_tc.store(value);
+      return PA_OK;
+    case PA_OPT_CASCADE_OVERLAP:
+      g_cascade_overlap.store(value ? 1 : 0);
       return PA_OK;
     case PA_OPT_DECODE_TOKEN_MAJOR:
       g_token_major.store(value ? 1 : 0);

@@ -207,8 +207,10 @@ struct PrefillLaunch {
   int num_tokens, num_q_heads, num_kv_heads, head_dim, num_blocks, bt_stride;
   float scale_log2;
   // overlapped mixed batch: header->prefill_ctas CTAs take the items and the
-  // grid releases the split-KV grid as soon as it has read that count
-  int overlap;
+  // grid releases the split-KV grid as soon as it has read that count.
+  // Overlapped cascade (prefix pass): prefix_ctas CTAs take the items, and the
+  // grid releases the suffix split-KV grid once the planner has completed.
+  int overlap, prefix_ctas;
   unsigned long long* err;
 };
 
@@ -245,11 +247,14 @@ struct DecodeParams {
   // scales (WsLayout::qsplit_off, qinv_off), written by launch_qsplit
   const unsigned char* qsplit;
   const float* qinv;
-  // overlapped mixed batch: this grid starts while the prefill-chunk grid
-  // still runs (its predecessor's predecessor, the planner, is complete);
-  // the worker count comes from the header and the grid completes only after
-  // the prefill-chunk grid
+  // overlapped mixed batch / cascade: this grid starts while the tensor-core
+  // grid before it (prefill chunks / cascade prefix pass) still runs (the
+  // planner, its predecessor's predecessor, is complete); the grid completes
+  // only after that grid. Mixed batch: the worker count comes from the header.
   int overlap;
+  // overlapped cascade: every (token, kv head) leaves partials, whole ones
+  // too; the merge pass folds them with the prefix partials (MergeParams::all_units)
+  int fold_later;
   unsigned long long* err;
 };
 
@@ -267,6 +272,11 @@ struct MergeParams {
   int slot_floats;
   int num_workers;  // split-KV workers launched (the slicing's upper bound)
   int workers_from_header;  // overlapped mixed batch: header->decode_workers, if fewer
+  // overlapped cascade: one CTA per (unit, kv head), merging that portion's
+  // suffix partials (the workers holding it, from the unit table) and the
+  // prefix chunks; grid units * Hkv
+  int all_units;
+  const UnitInfo* units;
   int token_major;          // token-major split-KV: a task {token, -, wf, wl} covers every
                             // kv head (CTA blockIdx = boundary * Hkv + kv head), slot
                             // (token + w) * Hkv + kv head

@@ -278,6 +278,13 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
   // the others retire at once and leave their SMs to the split-KV grid,
   // which every CTA releases here rather than on completion
   int ctas = (int)gridDim.x;
+  // Overlapped cascade: the prefix pass runs on a few SMs beside the suffix
+  // split-KV grid, which needs the plan. One warp (the last softmax warp,
+  // idle until the first scores) waits for the planner and then releases it.
+  if (PREFIX && p.overlap && warp == 1 + kSoftWarps) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   if (!PREFIX && p.overlap) {
     const int c = __ldcg(&p.header->prefill_ctas);
     if (c > 0 && c < ctas) {
@@ -696,9 +703,12 @@ __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreads, 1)
     // not complete before the planner (and the KV write before it) has, so a
     // dependent that waits for this grid sees the plan too. (The prefill-chunk
     // grid releases its dependent only by completing: triggering here too
-    // measured 0.53 vs 0.435 ms per mixed step.)
-    griddep_launch_dependents();
-    griddep_wait();
+    // measured 0.53 vs 0.435 ms per mixed step.) Overlapped, it did both at
+    // the top.
+    if (!p.overlap) {
+      griddep_launch_dependents();
+      griddep_wait();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -817,11 +827,13 @@ cudaError_t launch_prefill_t(const PrefillLaunch& a, int num_sms, cudaStream_t s
   p.k_cache8 = F8 ? static_cast<const unsigned char*>(a.k_cache) : nullptr;
   p.v_cache8 = F8 ? static_cast<const unsigned char*>(a.v_cache) : nullptr;
   p.v_scale = F8 ? a.v_scale : 1.f;
-  p.overlap = PREFIX ? 0 : a.overlap;
+  p.overlap = a.overlap;
   int grid = num_sms;
   if (PREFIX) {
     const int items = p.prefix_pairs * a.num_kv_heads * a.prefix_chunks;
     grid = items < num_sms ? items : num_sms;
+    // overlapped cascade: the pass keeps to its share of the SMs
+    if (a.overlap && a.prefix_ctas > 0 && a.prefix_ctas < grid) grid = a.prefix_ctas;
   }
 
   auto kern = pa_prefill_kernel<D, G, PREFIX, F8>;

@@ -70,6 +70,24 @@ def test_cascade_matches_plain_attention_on_gpu():
     assert (plain - casc).abs().max().item() <= gu.MAX_ABS
 
 
+@pytest.mark.parametrize("overlap", [0, 1])
+def test_prefix_pass_beside_suffix_pass(overlap):
+    # the prefix pass on a few SMs beside the suffix pass (every (token, kv
+    # head) folded by the merge pass), or first (folded by the suffix pass):
+    # both match the oracle, and each other
+    w = wl.make_config(4)
+    binding.set_option("cascade_overlap", overlap)
+    try:
+        b, out = run_case(w, w.shared_prefix_blocks * 16, f"prefix-share cascade, overlap {overlap}")
+        binding.set_option("cascade_overlap", 1 - overlap)
+        other = cascade(b, w.shared_prefix_blocks * 16, out=torch.empty_like(b.q)).float()
+        torch.cuda.synchronize()
+        gu.check_no_device_error()
+        assert (out.float() - other).abs().max().item() <= gu.MAX_ABS
+    finally:
+        binding.set_option("cascade_overlap", 1)
+
+
 CASES = [
     # (ctx_lens, q_lens, Hq, Hkv, D, shared prefix blocks)
     ([40, 17, 90], [1, 1, 1], 8, 2, 128, 1),                   # 16-key prefix, one partial tile
