@@ -52,7 +52,18 @@ struct pa_block_pool {
   std::vector<int> ref, prev, next;
   std::vector<uint8_t> in_free, has_hash;
   std::vector<pa_host::Hash> hash;
-  std::unordered_map<pa_host::Hash, int, pa_host::HashKey> by_hash;
+  // The prefix cache's hash -> block map: open addressing with linear probing
+  // over a power-of-two table at least twice the block count (so a probe
+  // always reaches an empty slot). A slot holds a block index (-1: empty) and
+  // the low 32 bits of its digest's first word, which give the home slot and
+  // screen a probe before it reads the block's full digest. has_hash[i] is
+  // set exactly while block i is in the table. No allocation after creation.
+  struct Slot {
+    int32_t block;
+    uint32_t tag;
+  };
+  std::vector<Slot> table;
+  size_t mask = 0;
   int head = -1, tail = -1, num_free = 0;
 
   int find(int32_t pid) const {
@@ -62,7 +73,10 @@ struct pa_block_pool {
   void push_back(int i);
   void push_front(int i);
   void unlink(int i);
-  void drop_hash(int i);
+  static uint32_t tag_of(const pa_host::Hash& h) { return (uint32_t)pa_host::HashKey()(h); }
+  int lookup(const pa_host::Hash& h) const;   // block index holding h, or -1
+  bool insert(const pa_host::Hash& h, int i);  // false (nothing changed) if h is present
+  void drop_hash(int i);                       // take block i's digest out, if it has one
   // Internal forms used by the scheduler (indices, no validation).
   int pop_front_for_use();  // allocate one block: ref 1, hash dropped
   void release(int i);      // one reference; count 0 -> free queue

@@ -40,10 +40,41 @@ void pa_block_pool::unlink(int i) {
   --num_free;
 }
 
+int pa_block_pool::lookup(const Hash& h) const {
+  const uint32_t tag = tag_of(h);
+  for (size_t s = tag & mask;; s = (s + 1) & mask) {
+    const Slot e = table[s];
+    if (e.block < 0) return -1;
+    if (e.tag == tag && hash[e.block] == h) return e.block;
+  }
+}
+
+bool pa_block_pool::insert(const Hash& h, int i) {
+  const uint32_t tag = tag_of(h);
+  size_t s = tag & mask;
+  for (; table[s].block >= 0; s = (s + 1) & mask)
+    if (table[s].tag == tag && hash[table[s].block] == h) return false;  // first block keeps it
+  table[s] = Slot{i, tag};
+  hash[i] = h;
+  has_hash[i] = 1;
+  return true;
+}
+
 void pa_block_pool::drop_hash(int i) {
   if (!has_hash[i]) return;
-  auto it = by_hash.find(hash[i]);
-  if (it != by_hash.end() && it->second == i) by_hash.erase(it);
+  size_t hole = tag_of(hash[i]) & mask;
+  while (table[hole].block != i) hole = (hole + 1) & mask;
+  // Backward-shift deletion: walk the run after the hole and move back every
+  // entry whose home slot does not lie strictly between the hole and it, so
+  // no probe sequence crosses an empty slot before reaching its key.
+  for (size_t t = (hole + 1) & mask; table[t].block >= 0; t = (t + 1) & mask) {
+    const size_t home = table[t].tag & mask;
+    if (((t - home) & mask) >= ((t - hole) & mask)) {
+      table[hole] = table[t];
+      hole = t;
+    }
+  }
+  table[hole] = Slot{-1, 0};
   has_hash[i] = 0;
 }
 
@@ -82,6 +113,10 @@ pa_block_pool* pa_pool_create(int num_blocks, int block_size, const int32_t* ids
     p->in_free.assign(num_blocks, 0);
     p->has_hash.assign(num_blocks, 0);
     p->hash.resize(num_blocks);
+    size_t slots = 2;
+    while (slots < 2 * (size_t)num_blocks) slots *= 2;
+    p->table.assign(slots, pa_block_pool::Slot{-1, 0});
+    p->mask = slots - 1;
     p->index.reserve(num_blocks);
     for (int i = 0; i < num_blocks; ++i) {
       const int32_t pid = ids ? ids[i] : i;
@@ -138,10 +173,7 @@ pa_status pa_pool_cache_block(pa_block_pool* pool, int32_t id, const uint8_t has
   if (i < 0 || pool->ref[i] == 0 || pool->has_hash[i]) return PA_ERR_INVALID_ARG;
   Hash h;
   std::memcpy(h.data(), hash, 32);
-  if (pool->by_hash.count(h)) return PA_OK;  // first block keeps the hash
-  pool->by_hash.emplace(h, i);
-  pool->hash[i] = h;
-  pool->has_hash[i] = 1;
+  pool->insert(h, i);  // a digest already present stays with its first block
   return PA_OK;
 }
 
@@ -149,8 +181,8 @@ int32_t pa_pool_lookup(const pa_block_pool* pool, const uint8_t hash[32]) {
   if (!pool || !hash) return -1;
   Hash h;
   std::memcpy(h.data(), hash, 32);
-  auto it = pool->by_hash.find(h);
-  return it == pool->by_hash.end() ? -1 : pool->id[it->second];
+  const int i = pool->lookup(h);
+  return i < 0 ? -1 : pool->id[i];
 }
 
 int pa_pool_ref_count(const pa_block_pool* pool, int32_t id) {
@@ -185,9 +217,9 @@ int pa_pool_find_cached_prefix(const pa_block_pool* pool, const int32_t* tokens,
   for (int b = 0; b < limit; ++b) {
     parent = pa_host::block_hash(b ? &parent : nullptr, tokens + (size_t)b * bs, bs, extra,
                                  extra_len);
-    auto it = pool->by_hash.find(parent);
-    if (it == pool->by_hash.end()) break;  // a chained hash cannot match past a miss
-    out_ids[hits++] = pool->id[it->second];
+    const int i = pool->lookup(parent);
+    if (i < 0) break;  // a chained hash cannot match past a miss
+    out_ids[hits++] = pool->id[i];
   }
   return hits * bs;
 }

@@ -27,6 +27,7 @@ struct Req {
   std::vector<uint8_t> extra;   // extra hash keys
   int num_computed = 0;
   std::vector<int> blocks;      // pool indices, logical block order
+  std::vector<int32_t> ids;     // the same blocks' physical ids (block-table rows)
   std::vector<Hash> hashes;     // chained hashes of the first full blocks
   int num_registered = 0;       // leading blocks already registered or hit
   bool running = false;
@@ -55,9 +56,15 @@ struct pa_scheduler {
     }
   }
 
+  void add_block(Req* r, int i) {
+    r->blocks.push_back(i);
+    r->ids.push_back(pool->id[i]);
+  }
+
   void release_blocks(Req* r) {
     for (auto it = r->blocks.rbegin(); it != r->blocks.rend(); ++it) pool->release(*it);
     r->blocks.clear();
+    r->ids.clear();
     r->num_registered = 0;
   }
 
@@ -76,10 +83,7 @@ struct pa_scheduler {
     ensure_hashes(r, full);
     for (int b = r->num_registered; b < full; ++b) {
       const int i = r->blocks[b];
-      if (pool->has_hash[i] || pool->by_hash.count(r->hashes[b])) continue;
-      pool->by_hash.emplace(r->hashes[b], i);
-      pool->hash[i] = r->hashes[b];
-      pool->has_hash[i] = 1;
+      if (!pool->has_hash[i]) pool->insert(r->hashes[b], i);  // a present digest stays put
     }
     r->num_registered = full;
   }
@@ -198,7 +202,7 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
       }
     }
     if (self_preempted) break;
-    for (int k = 0; k < need; ++k) r->blocks.push_back(pool->pop_front_for_use());
+    for (int k = 0; k < need; ++k) s->add_block(r, pool->pop_front_for_use());
     sched.emplace_back(r, n);
     budget -= n;
     ++i;
@@ -213,9 +217,9 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
       const int max_hit = ((int)r->tokens.size() - 1) / bs;
       s->ensure_hashes(r, max_hit);
       for (int b = 0; b < max_hit; ++b) {
-        auto it = pool->by_hash.find(r->hashes[b]);
-        if (it == pool->by_hash.end()) break;
-        hits.push_back(it->second);
+        const int i = pool->lookup(r->hashes[b]);
+        if (i < 0) break;
+        hits.push_back(i);
       }
     }
     const int cached = (int)hits.size() * bs;
@@ -227,10 +231,12 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
     int evictable = 0;  // free cached blocks that a hit takes out of the queue
     for (int h : hits) evictable += pool->ref[h] == 0;
     if (need + evictable > pool->num_free) break;
-    for (int h : hits) pool->acquire(h);
-    r->blocks = hits;
+    for (int h : hits) {
+      pool->acquire(h);
+      s->add_block(r, h);
+    }
     r->num_registered = (int)hits.size();
-    for (int k = 0; k < need; ++k) r->blocks.push_back(pool->pop_front_for_use());
+    for (int k = 0; k < need; ++k) s->add_block(r, pool->pop_front_for_use());
     r->num_computed = cached;
     r->running = true;
     s->waiting.pop_front();
@@ -253,14 +259,14 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
     out->query_start_loc[k] = t;
     out->seq_lens[k] = ctx + n;
     int32_t* row = out->block_tables + (size_t)k * stride;
-    const int nb = (int)r->blocks.size();
-    for (int b = 0; b < nb; ++b) row[b] = pool->id[r->blocks[b]];
-    for (int b = nb; b < stride; ++b) row[b] = -1;
+    const int nb = (int)r->ids.size();
+    std::memcpy(row, r->ids.data(), (size_t)nb * sizeof(int32_t));
+    std::memset(row + nb, 0xFF, (size_t)(stride - nb) * sizeof(int32_t));  // -1 past the blocks
     for (int j = 0; j < n; ++j) {
       const int p = ctx + j;
       out->positions[t + j] = p;
       out->input_tokens[t + j] = r->tokens[p];
-      out->slot_mapping[t + j] = (int64_t)pool->id[r->blocks[p / bs]] * bs + p % bs;
+      out->slot_mapping[t + j] = (int64_t)r->ids[p / bs] * bs + p % bs;
     }
     t += n;
     max_q = std::max(max_q, n);
@@ -316,8 +322,8 @@ int pa_sched_request_blocks(const pa_scheduler* s, int64_t req_id, int32_t* out,
   auto it = s->reqs.find(req_id);
   if (it == s->reqs.end()) return PA_ERR_INVALID_ARG;
   const Req* r = it->second.get();
-  for (int b = 0; b < (int)r->blocks.size() && b < max; ++b)
-    if (out) out[b] = s->pool->id[r->blocks[b]];
+  for (int b = 0; b < (int)r->ids.size() && b < max; ++b)
+    if (out) out[b] = r->ids[b];
   return (int)r->blocks.size();
 }
 

@@ -374,6 +374,63 @@ def test_scheduler_rejects_bad_calls(host):
         s.finish(0)
 
 
+def test_prefix_map_under_colliding_digests(host):
+    """The prefix-cache map against a dict, with digests crowded into a few
+    home slots (the map's home slot is taken from a digest's first bytes;
+    0 and the last slot test the wrap-around), through registrations, hits
+    that pull a free block back, and evictions by allocation (the free
+    queue's head loses its digest), so long probe runs form and are cut by
+    deletions."""
+    n = 64  # a table of 128 slots
+    pool = host.BlockPool(num_blocks=n, block_size=16)
+    rng = np.random.default_rng(11)
+
+    def digest():
+        home = int(rng.choice([0, 1, 2, 127, 64]))
+        first = (int(rng.integers(0, 2**24)) << 7) | home  # same low 7 bits
+        rest = rng.integers(0, 256, 28, dtype=np.uint8).tobytes()
+        return first.to_bytes(4, "little") + rest
+
+    by_hash, of_block, live = {}, {}, []
+    for _ in range(3000):
+        op = rng.integers(0, 4)
+        if op == 0 and pool.num_free() > 0:  # allocate: the head blocks lose their digests
+            k = int(rng.integers(1, min(4, pool.num_free()) + 1))
+            head = pool.free_queue()[:k]
+            got = pool.allocate(k)
+            assert got == head
+            for b in got:
+                h = of_block.pop(b, None)
+                if h is not None:
+                    del by_hash[h]
+            live += got
+        elif op == 1 and live:  # register a referenced, unregistered block
+            b = live[int(rng.integers(0, len(live)))]
+            if b in of_block:
+                continue
+            h = digest() if rng.random() < 0.8 or not by_hash else list(by_hash)[0]
+            pool.cache_block(b, h)
+            if h not in by_hash:
+                by_hash[h] = b
+                of_block[b] = h
+        elif op == 2 and live:  # release one reference
+            b = live.pop(int(rng.integers(0, len(live))))
+            pool.release([b])
+        elif op == 3 and by_hash:  # a hit takes a reference (and the block off the queue)
+            h = list(by_hash)[int(rng.integers(0, len(by_hash)))]
+            b = pool.lookup(h)
+            assert b == by_hash[h]
+            pool.touch([b])
+            live.append(b)
+        for h, b in by_hash.items():
+            assert pool.lookup(h) == b
+        for b in range(n):
+            assert pool.is_cached(b) == (b in of_block)
+    assert len(by_hash) > 8  # the run kept a crowded map
+    for h in [digest() for _ in range(50)]:
+        assert pool.lookup(h) == by_hash.get(h, -1)
+
+
 # ---------------------------------------- invariants and random parity ----
 
 class KVModel:
