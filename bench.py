@@ -57,22 +57,24 @@ FALLBACK_HBM_GBS = 6800.0
 # ---------------------------------------------------------------------------
 # algorithmic work of one step (what a perfect implementation must move)
 # ---------------------------------------------------------------------------
-def step_bytes(w: wl.Workload) -> dict:
-    """Bytes one step must move at minimum (no re-reads, no partials)."""
+def step_bytes(w: wl.Workload, fp8: bool = False) -> dict:
+    """Bytes one step must move at minimum (no re-reads, no partials); with
+    fp8, the cache holds one-byte E4M3 codes instead of bf16."""
     D, Hq, Hkv, T = w.head_dim, w.num_q_heads, w.num_kv_heads, w.num_tokens
     L = w.seq_lens.astype(np.int64)
     nb = (L + 15) // 16
-    kv = int((L * Hkv * D * 2 * 2).sum())          # K and V rows, bf16
+    eb = 1 if fp8 else 2                            # bytes per cached element
+    kv = int((L * Hkv * D * 2 * eb).sum())          # K and V rows
     if w.shared_prefix_blocks:
         # unique bytes: the shared prefix blocks are stored (and need reading) once
         P = w.shared_prefix_blocks
-        kv_unique = kv - (w.num_reqs - 1) * P * 16 * Hkv * D * 2 * 2
+        kv_unique = kv - (w.num_reqs - 1) * P * 16 * Hkv * D * 2 * eb
     else:
         kv_unique = kv
     qo = 2 * T * Hq * D * 2                         # q in, out out
     meta = int(nb.sum()) * 4 + w.num_reqs * 8 + 4
     attn = kv + qo + meta
-    write = 2 * T * Hkv * D * 2 * 2 + T * 8          # read k,v new; write cache rows
+    write = T * Hkv * D * 2 * (2 + eb) + T * 8      # read k,v new (bf16); write cache rows
     return {"kv": kv, "kv_unique": kv_unique, "attention": attn, "write": write,
             "step": attn + write}
 
@@ -469,9 +471,8 @@ def prefix_share_timing(args, flush, torch, binding, dist, rank, world) -> dict:
 def fp8_timing(args, flush, torch, binding, dist, rank, world, peaks) -> dict:
     """The headline decode batch with an E4M3 KV cache (per-tensor scales)."""
     w = wl.make_config(HEADLINE_CONFIG, seed=42 + HEADLINE_CONFIG + 1000 * rank)
-    sb = step_bytes(w)
-    kv8 = sb["kv"] // 2
-    attn8 = sb["attention"] - sb["kv"] + kv8
+    sb = step_bytes(w, fp8=True)
+    kv8, attn8 = sb["kv"], sb["attention"]
     steps = max(50, args.steps // 10)
     res = Resident(w, torch, binding, fp8_scales=FP8_SCALES)
     t = time_steps(res, steps, args.warmup, flush, torch, binding, dist)
@@ -564,6 +565,8 @@ def run_ours(args, rank, world, local, dist):
     binding.init()
     binding.get_device_error(clear=True)
     binding.set_option("decode_tc", {"auto": 1, "cuda-core": 0, "tensor-core": 2}[args.split_kv])
+    if args.tm_ctas_per_sm:
+        binding.set_option("decode_tm_ctas_per_sm", args.tm_ctas_per_sm)
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
@@ -584,7 +587,7 @@ def run_ours(args, rank, world, local, dist):
         casc = w.shared_prefix_blocks * 16 if (args.cascade and idx == args.config) else 0
         f8 = FP8_SCALES if (args.fp8 and idx == args.config) else None
         res = Resident(w, torch, binding, cascade_len=casc, fp8_scales=f8)
-        sb = step_bytes(w)
+        sb = step_bytes(w, fp8=f8 is not None)
         steps = args.steps if idx == args.config else max(50, args.steps // 10)
         t = time_steps(res, steps, args.warmup, flush, torch, binding, dist,
                        clocks=ClockSampler(local) if idx == args.config else None)
@@ -633,10 +636,12 @@ def run_ours(args, rank, world, local, dist):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3" if args.fp8 else "bf16",
         "data": "synthetic (seeded numpy PCG64, N(0,1) rounded to bf16)",
         "config": {"workload": f"{wl.CONFIG_NAMES[args.config]}: "
-                               f"{wl.CONFIG_DESCRIPTIONS[args.config]}",
+                               f"{wl.CONFIG_DESCRIPTIONS[args.config]}" +
+                               (f" over an E4M3 KV cache (k_scale {FP8_SCALES[0]}, "
+                                f"v_scale {FP8_SCALES[1]})" if args.fp8 else ""),
                    "num_reqs": w.num_reqs, "num_tokens": w.num_tokens,
                    "split_kv": args.split_kv,
                    "step_signature": main["signature"],
@@ -834,6 +839,9 @@ def main():
     ap.add_argument("--split-kv", choices=["auto", "cuda-core", "tensor-core"], default="auto",
                     help="split-KV kernel: the library's routing (default), or one forced "
                          "(pa_set_option PA_OPT_DECODE_TC 0 / 2)")
+    ap.add_argument("--tm-ctas-per-sm", type=int, choices=[1, 2], default=None,
+                    help="CTAs per SM of the token-major E4M3 split-KV kernel "
+                         "(pa_set_option PA_OPT_DECODE_TM_CTAS_PER_SM; default: the library's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -383,6 +383,15 @@ pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event
  *     differs). value 0: the prefix pass first, folded by the suffix pass.
  */
 #define PA_OPT_CASCADE_OVERLAP 6
+/*
+ *   PA_OPT_DECODE_TM_CTAS_PER_SM (default 2; 1 or 2, anything else is
+ *     PA_ERR_INVALID_ARG): CTAs per SM of the token-major E4M3 kernel. With 2
+ *     (taken only at G = Hq / Hkv <= 4; G = 8 always runs one) each SM runs
+ *     two CTAs of two copy stages each instead of one of four, so twice as
+ *     many workers slice the keys; results stay within the attention
+ *     tolerances.
+ */
+#define PA_OPT_DECODE_TM_CTAS_PER_SM 7
 pa_status pa_set_option(int option, int value);
 
 /* Number of kernel launches the library has issued in this process. */

@@ -82,11 +82,13 @@ constexpr int kTmD = 128;    // head dim
 constexpr int kTmHkv = 8;    // KV heads: 8 x 16 keys = the MMA's 128 rows
 constexpr int kTmThreads = 192;
 
-template <int G>
+template <int G, int CPS>
 struct TmL {
   static constexpr int HQ = kTmHkv * G;          // query heads of a token
   static constexpr int N = 2 * HQ;               // MMA N: hi rows, then lo rows
-  static constexpr int kStages = G == 8 ? 3 : 4;
+  // CTAs resident per SM: two (G <= 4) take two stages each, so an SM holds
+  // the same bytes in flight in two independent per-tile chains
+  static constexpr int kStages = CPS == 2 ? 2 : (G == 8 ? 3 : 4);
   static constexpr int kKvTile = 16384;          // one block, all KV heads: [128 rows][128 B]
   static constexpr int kQBytes = N * 128;        // a token's q' rows: [hi, lo][HQ rows][128 B]
   static constexpr int kStageBytes = 2 * kKvTile + kQBytes;
@@ -107,10 +109,13 @@ struct TmL {
   static constexpr int OFF_TSLOT = OFF_BAR + 8 * B_COUNT;
   static constexpr int OFF_UNITS = (OFF_TSLOT + 16 + 15) / 16 * 16;  // self-planned unit table
   static constexpr int SMEM = OFF_UNITS + (int)sizeof(UnitInfo) * (kSelfPlanMaxReqs + 1) + 1024;
-  static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+  static_assert(CPS == 1 || CPS == 2, "one or two CTAs per SM");
+  // 228 KB of shared memory per SM, 1 KB of it reserved per resident CTA
+  static_assert(SMEM <= (CPS == 1 ? 227 * 1024 : 113 * 1024), "CTAs per SM fit in shared memory");
   static_assert(kStageBytes % 1024 == 0 && kPBytes % 1024 == 0, "1024-byte aligned operand tiles");
   // TMEM columns: S^T buffers at 0 and N, O^T buffers at 2N and 3N
   static constexpr uint32_t kTmemCols = 4 * N;
+  static_assert(CPS * kTmemCols <= 512, "the resident CTAs' TMEM fits in 512 columns");
   static constexpr int CW = HQ < 16 ? HQ : 16;  // O^T columns per TMEM load in epilogues
 };
 
@@ -149,10 +154,10 @@ struct TmDecodeParams {
   DecodeParams d;
 };
 
-template <int G>
-__global__ void __launch_bounds__(kTmThreads, 1)
+template <int G, int CPS>
+__global__ void __launch_bounds__(kTmThreads, CPS)
     pa_decode_tm_kernel(const __grid_constant__ TmDecodeParams tp) {
-  using L = TmL<G>;
+  using L = TmL<G, CPS>;
   constexpr int HQ = L::HQ, N = L::N, kStages = L::kStages;
   const DecodeParams& p = tp.d;
   extern __shared__ unsigned char smem_raw[];
@@ -751,9 +756,9 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 // ---------------------------------------------------------------------------------------
 namespace {
 
-template <int G>
+template <int G, int CPS>
 cudaError_t launch_tm_t(const DecodeParams& d, int grid, cudaStream_t s) {
-  using L = TmL<G>;
+  using L = TmL<G, CPS>;
   TmDecodeParams tp;
   tp.d = d;
   const uint64_t qrows = (uint64_t)d.num_tokens * (uint64_t)d.num_q_heads;
@@ -770,13 +775,17 @@ cudaError_t launch_tm_t(const DecodeParams& d, int grid, cudaStream_t s) {
       !encode_tmap_u8(&tp.tm_k, 2, d.k_cache, cd, cs, cb) ||
       !encode_tmap_u8(&tp.tm_v, 2, d.v_cache, cd, cs, cb))
     return cudaErrorInvalidValue;
-  auto kern = pa_decode_tm_kernel<G>;
+  auto kern = pa_decode_tm_kernel<G, CPS>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (e != cudaSuccess) return e;
+    // the whole unified on-chip memory as shared memory, so CPS CTAs fit
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -797,6 +806,12 @@ cudaError_t launch_tm_t(const DecodeParams& d, int grid, cudaStream_t s) {
 
 }  // namespace
 
+int decode_tm_workers(int group, int num_sms, int ctas_per_sm) {
+  const int cps = (ctas_per_sm == 2 && group <= 4) ? 2 : 1;
+  const int w = cps * num_sms;
+  return w < kMaxDecodeWorkers / kTmHkv ? w : kMaxDecodeWorkers / kTmHkv;
+}
+
 bool decode_tm_supported(int head_dim, int group, int num_kv_heads, int workers) {
   return head_dim == kTmD && num_kv_heads == kTmHkv &&
          (group == 1 || group == 2 || group == 4 || group == 8) &&
@@ -805,15 +820,16 @@ bool decode_tm_supported(int head_dim, int group, int num_kv_heads, int workers)
          workers * kTmHkv <= kMaxDecodeWorkers;
 }
 
-cudaError_t launch_decode_tm(const DecodeParams& p, int group, int num_sms, cudaStream_t s,
-                             int* workers_out) {
-  const int grid = num_sms < kMaxDecodeWorkers ? num_sms : kMaxDecodeWorkers;
+cudaError_t launch_decode_tm(const DecodeParams& p, int group, int num_sms, int ctas_per_sm,
+                             cudaStream_t s, int* workers_out) {
+  const int grid = decode_tm_workers(group, num_sms, ctas_per_sm);
   *workers_out = grid;
+  const bool two = grid > num_sms;  // two CTAs per SM
   switch (group) {
-    case 1: return launch_tm_t<1>(p, grid, s);
-    case 2: return launch_tm_t<2>(p, grid, s);
-    case 4: return launch_tm_t<4>(p, grid, s);
-    case 8: return launch_tm_t<8>(p, grid, s);
+    case 1: return two ? launch_tm_t<1, 2>(p, grid, s) : launch_tm_t<1, 1>(p, grid, s);
+    case 2: return two ? launch_tm_t<2, 2>(p, grid, s) : launch_tm_t<2, 1>(p, grid, s);
+    case 4: return two ? launch_tm_t<4, 2>(p, grid, s) : launch_tm_t<4, 1>(p, grid, s);
+    case 8: return launch_tm_t<8, 1>(p, grid, s);
   }
   return cudaErrorInvalidValue;
 }

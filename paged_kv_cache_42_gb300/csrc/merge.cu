@@ -144,6 +144,96 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
   }
 }
 
+// Token-major split-KV (eight KV heads): one CTA per slice boundary, one warp
+// per KV head. A boundary's token leaves its partials in slots
+// (token + w) * Hkv + kv for the workers w = wf .. wl that hold its blocks -
+// usually two to a few dozen, so a warp merges its head's partials on its
+// own, online, loading them a group at a time; no shared memory and no block
+// barrier.
+template <int D, int G>
+__global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_tm_kernel(const MergeParams p) {
+  constexpr int V = D / 32;  // output dims per lane
+  static_assert(V == 2 || V == 4, "head dim 64 or 128");
+  griddep_wait();  // the split-KV grid's partials and tasks
+  const int W = __ldcg(&p.header->num_positions);
+  int nw = p.num_workers;
+  if (p.workers_from_header) nw = min(nw, __ldcg(&p.header->decode_workers));
+  if (W <= 0) return;
+  const int w = (int)blockIdx.x + 1;
+  const int4 task = __ldcg(p.tasks + w);
+  if (w >= plan_workers(W, nw) || task.x < 0) return;  // stale task past this call's workers
+  const int kv = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+  if (kv >= p.num_kv_heads) return;
+  const int tok = task.x, wf = task.z, n = task.w - task.z + 1;
+  auto slot = [&](int i) -> const float* {
+    return p.partials + ((size_t)(tok + wf + i) * p.num_kv_heads + kv) * p.slot_floats;
+  };
+  struct Part {
+    float m[G], l[G], o[G][V];
+  };
+  auto load = [&](int i, Part& q) {
+    const float* const sl = slot(i);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      q.m[h] = __ldcg(sl + h);
+      q.l[h] = __ldcg(sl + G + h);
+      if constexpr (V == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(sl + 16 + h * D) + lane);
+        q.o[h][0] = v.x;
+        q.o[h][1] = v.y;
+        q.o[h][2] = v.z;
+        q.o[h][3] = v.w;
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(sl + 16 + h * D) + lane);
+        q.o[h][0] = v.x;
+        q.o[h][1] = v.y;
+      }
+    }
+  };
+  // partials in groups of K: a group's loads are all issued before any of
+  // them is combined, so a group costs one round trip to L2
+  constexpr int K = G <= 4 ? 4 : 2;
+  Part acc, q[K];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    acc.m[h] = -INFINITY;
+    acc.l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc.o[h][e] = 0.f;
+  }
+  for (int i0 = 0; i0 < n; i0 += K) {
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+      if (i0 + k < n) load(i0 + k, q[k]);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      if (i0 + k >= n) break;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mn = fmaxf(acc.m[h], q[k].m[h]);
+        const float a = exp2f(acc.m[h] - mn), b = exp2f(q[k].m[h] - mn);  // acc.m = -inf: a = 0
+        acc.l[h] = acc.l[h] * a + q[k].l[h] * b;
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc.o[h][e] = acc.o[h][e] * a + q[k].o[h][e] * b;
+        acc.m[h] = mn;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float sc = p.v_scale / acc.l[h];
+    uint16_t* const orow = p.out + ((size_t)tok * p.num_q_heads + (size_t)kv * G + h) * D;
+    if constexpr (V == 4) {
+      const uint2 pk = make_uint2(float2_to_bf16x2(acc.o[h][0] * sc, acc.o[h][1] * sc),
+                                  float2_to_bf16x2(acc.o[h][2] * sc, acc.o[h][3] * sc));
+      *reinterpret_cast<uint2*>(orow + lane * V) = pk;
+    } else {
+      *reinterpret_cast<uint32_t*>(orow + lane * V) =
+          float2_to_bf16x2(acc.o[h][0] * sc, acc.o[h][1] * sc);
+    }
+  }
+}
+
 template <int D, int G>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
   // one CTA per slice boundary (and kv head), or per (token, kv head)
@@ -162,6 +252,12 @@ cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.token_major && !p.all_units && p.prefix_chunks == 0 &&
+      p.num_kv_heads <= kMergeWarps) {  // a CTA per boundary, a warp per KV head
+    cfg.gridDim = dim3((unsigned)(p.num_workers - 1));
+    cfg.blockDim = dim3(32 * p.num_kv_heads);
+    return cudaLaunchKernelEx(&cfg, pa_merge_tm_kernel<D, G>, p);
+  }
   return cudaLaunchKernelEx(&cfg, pa_merge_kernel<D, G>, p);
 }
 

@@ -43,6 +43,7 @@ std::atomic<int> g_max_workers{0};  // pa_set_option(PA_OPT_DECODE_MAX_WORKERS, 
 std::atomic<int> g_mixed_overlap{1};  // pa_set_option(PA_OPT_MIXED_OVERLAP, ...)
 std::atomic<int> g_token_major{1};  // pa_set_option(PA_OPT_DECODE_TOKEN_MAJOR, ...)
 std::atomic<int> g_cascade_overlap{1};  // pa_set_option(PA_OPT_CASCADE_OVERLAP, ...)
+std::atomic<int> g_tm_ctas{2};  // pa_set_option(PA_OPT_DECODE_TM_CTAS_PER_SM, ...)
 constexpr int kNumTimers = 6;  // write, plan, decode, prefill, cascade prefix, merge
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
@@ -331,15 +332,18 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
     if (prefix_ctas < 1) prefix_ctas = 1;
   }
   const int dec_sms = d->num_sms - prefix_ctas;  // SMs the split-KV grid fills
-  const int launched = use_tc ? decode_tc_workers(d->num_sms)
-                              : decode_workers(head_dim, pp.group, kv_fp8 != 0, dec_sms, occ_cap);
+  // An E4M3 cache over eight KV heads takes the token-major tiles (one block
+  // of every KV head per tile) on the tensor cores.
+  const int tm_cps = g_tm_ctas.load();
+  const bool use_tm =
+      use_tc && kv_fp8 && g_token_major.load() &&
+      decode_tm_supported(head_dim, group, num_kv_heads, decode_tm_workers(group, d->num_sms, tm_cps));
+  const int launched = use_tm   ? decode_tm_workers(group, d->num_sms, tm_cps)
+                       : use_tc ? decode_tc_workers(d->num_sms)
+                                : decode_workers(head_dim, pp.group, kv_fp8 != 0, dec_sms, occ_cap);
   if (launched <= 0) return PA_ERR_CUDA;
   const int cap = g_max_workers.load();
   pp.num_workers = (cap > 0 && cap < launched) ? cap : launched;
-  // An E4M3 cache over eight KV heads takes the token-major tiles (one block
-  // of every KV head per tile) on the tensor cores.
-  const bool use_tm = use_tc && kv_fp8 && g_token_major.load() &&
-                      decode_tm_supported(head_dim, group, num_kv_heads, launched);
   pp.token_major = use_tm ? 1 : 0;
   // A mixed batch on the tensor-core split-KV kernel (bf16) may run its
   // prefill chunks on a few SMs beside the split-KV work (the planner decides
@@ -440,7 +444,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   {
     TimerScope timer(2, s);
     const cudaError_t e =
-        use_tm   ? launch_decode_tm(dp, group, d->num_sms, s, &launched_workers)
+        use_tm   ? launch_decode_tm(dp, group, d->num_sms, tm_cps, s, &launched_workers)
         : use_tc ? launch_decode_tc(dp, group, kv_fp8 != 0, d->num_sms, s, &launched_workers)
                  : launch_decode(dp, head_dim, group, kv_fp8 != 0, dec_sms, occ_cap, s,
                                  &launched_workers);
@@ -568,6 +572,10 @@ pa_status pa_set_option(int option, int value) {
       return PA_OK;
     case PA_OPT_DECODE_TOKEN_MAJOR:
       g_token_major.store(value ? 1 : 0);
+      return PA_OK;
+    case PA_OPT_DECODE_TM_CTAS_PER_SM:
+      if (value != 1 && value != 2) return PA_ERR_INVALID_ARG;
+      g_tm_ctas.store(value);
       return PA_OK;
     case PA_OPT_MIXED_OVERLAP:
       g_mixed_overlap.store(value ? 1 : 0);

@@ -278,7 +278,7 @@ struct MergeParams {
   int all_units;
   const UnitInfo* units;
   int token_major;          // token-major split-KV: a task {token, -, wf, wl} covers every
-                            // kv head (CTA blockIdx = boundary * Hkv + kv head), slot
+                            // kv head (a CTA per boundary, a warp per kv head), slot
                             // (token + w) * Hkv + kv head
   int num_q_heads, num_kv_heads, num_tokens;
   int key_start_blocks;
@@ -350,9 +350,12 @@ cudaError_t launch_qsplit(const DecodeParams& p, int group, cudaStream_t s);
 // eight KV heads, head_dim 128. Its positions are (token, block) - the plan
 // built with PlanParams::token_major - and its partial of (token, kv head)
 // from worker w sits in slot (token + w) * 8 + kv head (MergeParams::token_major).
+// It runs ctas_per_sm (1 or 2; 2 only for G <= 4) CTAs per SM, one worker
+// each: decode_tm_workers of them.
+int decode_tm_workers(int group, int num_sms, int ctas_per_sm);
 bool decode_tm_supported(int head_dim, int group, int num_kv_heads, int workers);
-cudaError_t launch_decode_tm(const DecodeParams& p, int group, int num_sms, cudaStream_t s,
-                             int* workers_out);
+cudaError_t launch_decode_tm(const DecodeParams& p, int group, int num_sms, int ctas_per_sm,
+                             cudaStream_t s, int* workers_out);
 
 // 2-D tiled tensor map (CUtensorMap, passed as void*) over a row-major bf16
 // matrix of `rows` rows of `inner` elements, `row_stride_bytes` apart, with a

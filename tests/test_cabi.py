@@ -53,6 +53,16 @@ def test_version(pa_lib):
     assert pa_lib.pa_version() >= 100
 
 
+def test_set_option_validates_values(pa_lib):
+    # PA_OPT_DECODE_TM_CTAS_PER_SM takes 1 or 2 only; a valid value is kept
+    # until set again (restored here to the default, 2)
+    for v in (0, 3, -1):
+        assert pa_lib.pa_set_option(7, v) == -1  # PA_ERR_INVALID_ARG
+    assert pa_lib.pa_set_option(7, 1) == 0
+    assert pa_lib.pa_set_option(7, 2) == 0
+    assert pa_lib.pa_set_option(99, 1) == -1  # no such option
+
+
 def write(pa_lib, **kw):
     a = dict(k=FAKE, v=FAKE, slot=FAKE, kc=FAKE, vc=FAKE, T=4, hkv=2, d=64, bs=16, nb=8)
     a.update(kw)

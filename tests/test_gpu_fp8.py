@@ -161,12 +161,16 @@ TC_CASES = [
 ]
 
 
+TM_CPS_DEFAULT = 2  # PA_OPT_DECODE_TM_CTAS_PER_SM's default
+
+
 @pytest.fixture
 def decode_tc_option():
     yield binding.set_option
     binding.set_option("decode_tc", 1)
     binding.set_option("decode_max_workers", 0)
     binding.set_option("decode_token_major", 1)
+    binding.set_option("decode_tm_ctas_per_sm", TM_CPS_DEFAULT)
 
 
 @pytest.mark.parametrize("i", range(len(TC_CASES)))
@@ -198,8 +202,9 @@ def test_attention_fp8_tensor_core_running_max_and_splits(decode_tc_option):
     run(w, 0.03, 1.0, "fp8 tc running max, 5 parts")
 
 
+@pytest.mark.parametrize("cps", [1, 2])
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
-def test_token_major_running_max_and_splits(g, decode_tc_option):
+def test_token_major_running_max_and_splits(g, cps, decode_tc_option):
     # Eight KV heads whose scores grow along the sequence at head-dependent
     # rates: references move in some half-warps and not others (O^T columns
     # rescaled per query head); then the same over 1, 2 and 7 workers (token
@@ -215,15 +220,18 @@ def test_token_major_running_max_and_splits(g, decode_tc_option):
                 np.float32(rate * (p // 64)))
         w.k_new[0, kv] = wl.to_bf16_bits(np.float32(rate * ((L0 - 1) // 64)))
     decode_tc_option("decode_tc", 2)
-    run(w, 0.03, 1.0, f"fp8 token-major running max, G {g}")
+    decode_tc_option("decode_tm_ctas_per_sm", cps)  # 2: taken at G <= 4
+    run(w, 0.03, 1.0, f"fp8 token-major running max, G {g}, {cps} CTAs per SM")
     for n in (1, 2, 7):
         decode_tc_option("decode_max_workers", n)
         run(w, 0.03, 1.0, f"fp8 token-major running max, G {g}, {n} parts")
 
 
-def test_token_major_random_batches(decode_tc_option):
+@pytest.mark.parametrize("cps", [1, 2])
+def test_token_major_random_batches(cps, decode_tc_option):
     # decode-only batches (self-planned) and batches with short spans and
     # tensor-core chunks (planner path), at every group size
+    decode_tc_option("decode_tm_ctas_per_sm", cps)
     rng = np.random.default_rng(1190)
     for it in range(6):
         R = int(rng.integers(1, 50))
@@ -235,6 +243,23 @@ def test_token_major_random_batches(decode_tc_option):
         w = wl.make_workload(ctx, ql, num_q_heads=8 * g, num_kv_heads=8, head_dim=128,
                              seed=1191 + it, pool_factor=1.2)
         run(w, 0.0113, 0.0127, f"fp8 token-major random batch {it}")
+
+
+def test_token_major_two_ctas_per_sm_llama8b(decode_tc_option):
+    # the Llama-8B batch (G 4) on two CTAs per SM (304 workers on 152 SMs,
+    # the default): every row against the oracle, and close to the
+    # one-CTA-per-SM result
+    w = wl.make_config(2)
+    decode_tc_option("decode_tm_ctas_per_sm", 2)
+    run(w, 0.0113, 0.0127, "llama8b fp8, token-major, two CTAs per SM")
+    b = Fp8Batch(w, 0.0113, 0.0127)
+    b.write()
+    a = gu.to_f64(b.attend())
+    decode_tc_option("decode_tm_ctas_per_sm", 1)
+    c = gu.to_f64(b.attend())
+    torch.cuda.synchronize()
+    gu.check_no_device_error()
+    assert np.abs(a - c).max() <= gu.MAX_ABS
 
 
 def test_token_major_against_per_head_tiles(decode_tc_option):
