@@ -567,6 +567,8 @@ def run_ours(args, rank, world, local, dist):
     binding.set_option("decode_tc", {"auto": 1, "cuda-core": 0, "tensor-core": 2}[args.split_kv])
     if args.tm_ctas_per_sm:
         binding.set_option("decode_tm_ctas_per_sm", args.tm_ctas_per_sm)
+    if args.mixed_prefill_ctas:
+        binding.set_option("mixed_prefill_ctas", args.mixed_prefill_ctas)
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
@@ -842,6 +844,9 @@ def main():
     ap.add_argument("--tm-ctas-per-sm", type=int, choices=[1, 2], default=None,
                     help="CTAs per SM of the token-major E4M3 split-KV kernel "
                          "(pa_set_option PA_OPT_DECODE_TM_CTAS_PER_SM; default: the library's)")
+    ap.add_argument("--mixed-prefill-ctas", type=int, default=0,
+                    help="SMs the prefill chunks take beside the split-KV work in a mixed "
+                         "batch (pa_set_option PA_OPT_MIXED_PREFILL_CTAS; 0: the planner's)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

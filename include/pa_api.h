@@ -392,6 +392,15 @@ pa_status pa_set_kernel_timer(int kernel_id, void* start_event, void* stop_event
  *     tolerances.
  */
 #define PA_OPT_DECODE_TM_CTAS_PER_SM 7
+/*
+ *   PA_OPT_MIXED_PREFILL_CTAS (default 0; negative is PA_ERR_INVALID_ARG):
+ *     in an overlapped mixed batch (PA_OPT_MIXED_OVERLAP), how many SMs the
+ *     prefill chunks take beside the split-KV work. 0: the planner's cost
+ *     model decides, and may run the two in turn instead. n > 0: always
+ *     overlap, with min(n, SMs / 2) SMs for the chunks. Results do not depend
+ *     on it beyond the attention tolerances (the split-KV slicing changes).
+ */
+#define PA_OPT_MIXED_PREFILL_CTAS 8
 pa_status pa_set_option(int option, int value);
 
 /* Number of kernel launches the library has issued in this process. */

@@ -312,7 +312,7 @@ def set_kernel_timer(kernel: str, start: torch.cuda.Event | None,
     _check(lib().pa_set_kernel_timer(KERNEL_IDS[kernel], sp, ep), "pa_set_kernel_timer")
 
 
-OPTIONS = {"decode_self_plan": 1, "decode_tc": 2, "decode_max_workers": 3, "mixed_overlap": 4, "decode_token_major": 5, "cascade_overlap": 6, "decode_tm_ctas_per_sm": 7}
+OPTIONS = {"decode_self_plan": 1, "decode_tc": 2, "decode_max_workers": 3, "mixed_overlap": 4, "decode_token_major": 5, "cascade_overlap": 6, "decode_tm_ctas_per_sm": 7, "mixed_prefill_ctas": 8}
 
 
 def set_option(name: str, value: int) -> None:

@@ -44,6 +44,7 @@ std::atomic<int> g_mixed_overlap{1};  // pa_set_option(PA_OPT_MIXED_OVERLAP, ...
 std::atomic<int> g_token_major{1};  // pa_set_option(PA_OPT_DECODE_TOKEN_MAJOR, ...)
 std::atomic<int> g_cascade_overlap{1};  // pa_set_option(PA_OPT_CASCADE_OVERLAP, ...)
 std::atomic<int> g_tm_ctas{2};  // pa_set_option(PA_OPT_DECODE_TM_CTAS_PER_SM, ...)
+std::atomic<int> g_mixed_ctas{0};  // pa_set_option(PA_OPT_MIXED_PREFILL_CTAS, ...): 0 = planned
 constexpr int kNumTimers = 6;  // write, plan, decode, prefill, cascade prefix, merge
 cudaEvent_t g_timer_start[kNumTimers] = {};
 cudaEvent_t g_timer_stop[kNumTimers] = {};
@@ -350,6 +351,7 @@ pa_status attention_impl(const void* q, const void* k_cache, const void* v_cache
   // how many, or none); the E4M3 path keeps its query-split pass between them.
   const int overlap = (g_mixed_overlap.load() && pp.use_prefill && use_tc && !kv_fp8) ? 1 : 0;
   pp.overlap = overlap;
+  pp.prefill_ctas_override = g_mixed_ctas.load();
   pp.num_sms = d->num_sms;
   pp.position_bytes = 2 * kBlockSize * head_dim * 2;  // K and V of one 16-key block
   pp.header = reinterpret_cast<WsHeader*>(ws + lay.header_off);
@@ -576,6 +578,10 @@ pa_status pa_set_option(int option, int value) {
     case PA_OPT_DECODE_TM_CTAS_PER_SM:
       if (value != 1 && value != 2) return PA_ERR_INVALID_ARG;
       g_tm_ctas.store(value);
+      return PA_OK;
+    case PA_OPT_MIXED_PREFILL_CTAS:
+      if (value < 0) return PA_ERR_INVALID_ARG;
+      g_mixed_ctas.store(value);
       return PA_OK;
     case PA_OPT_MIXED_OVERLAP:
       g_mixed_overlap.store(value ? 1 : 0);

@@ -176,6 +176,7 @@ struct PlanParams {
   // prefill-chunk and split-KV grids (num_sms of them; position_bytes of
   // K and V per split-KV position)
   int overlap, num_sms, position_bytes;
+  int prefill_ctas_override;  // > 0: the prefill-chunk grid's share, instead of the cost model
   int token_major;  // positions per token are its blocks (all kv heads at once)
   WsHeader* header;
   UnitInfo* units;

@@ -215,7 +215,10 @@ __global__ void __launch_bounds__(kPlanThreads) pa_plan_kernel(PlanParams p) {
       const float c2 = pre * kHbmBytesPerUs / (kOverlapMargin * bytes);
       const int c = max(1, (int)ceilf(fminf(fminf(c1, c2), (float)S_)));
       const float serial = 1.6f * pre / (float)S_ + dec_us(S_);
-      if (c <= S_ / 4 && dec_us(S_ - c) < serial) {
+      if (p.prefill_ctas_override > 0) {  // the caller's share (at most half the SMs)
+        ctas = min(p.prefill_ctas_override, S_ / 2);
+        workers = min(workers, S_ - ctas);
+      } else if (c <= S_ / 4 && dec_us(S_ - c) < serial) {
         ctas = c;
         workers = min(workers, S_ - c);
       }

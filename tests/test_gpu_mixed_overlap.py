@@ -34,6 +34,7 @@ def _lib():
     binding.get_device_error(clear=True)
     yield
     binding.set_option("mixed_overlap", 1)
+    binding.set_option("mixed_prefill_ctas", 0)
 
 
 @contextlib.contextmanager
@@ -137,3 +138,32 @@ def test_overlapped_step_is_deterministic_and_split_count_capped():
     reqs = chunks + decodes[:20]
     rows = gu.rows_of(w, reqs)
     gu.assert_close(c[rows], gu.oracle_reference(w, reqs=reqs)[rows], "overlap, 7 workers")
+
+
+@pytest.mark.parametrize("n", [1, 12, 40, 10000])
+def test_forced_prefill_share(n):
+    # PA_OPT_MIXED_PREFILL_CTAS: the chunks take min(n, SMs / 2) SMs whatever
+    # the cost model says, even on the chunk-heavy batch it keeps serial
+    S = _num_sms()
+    for w in (wl.make_config(3),
+              wl.make_workload([4096, 3000, 40, 300], [512, 512, 1, 1], num_q_heads=32,
+                               num_kv_heads=8, head_dim=128, seed=2130)):
+        ser, _, _ = _run(w, False)
+        binding.set_option("mixed_prefill_ctas", n)
+        try:
+            got, ctas, workers = _run(w, True)
+        finally:
+            binding.set_option("mixed_prefill_ctas", 0)
+        assert ctas == min(n, S // 2) and workers == S - ctas, (n, ctas, workers)
+        chunks, decodes = _chunk_and_decode_rows(w)
+        crow = gu.rows_of(w, chunks)
+        assert np.array_equal(got[crow], ser[crow])  # the same items on either path
+        reqs = chunks + decodes[:20] + decodes[-20:]
+        rows = gu.rows_of(w, reqs)
+        gu.assert_close(got[rows], gu.oracle_reference(w, reqs=reqs)[rows],
+                        f"{n} prefill CTAs")
+
+
+def test_bad_prefill_share_rejected():
+    with pytest.raises(RuntimeError):
+        binding.set_option("mixed_prefill_ctas", -1)
