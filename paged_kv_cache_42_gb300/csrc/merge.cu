@@ -51,26 +51,23 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_kernel(const MergeP
     wf = worker_of(first, W, NW);
     wl = worker_of(first + nb - 1, W, NW);
   } else {
-    // token-major split-KV: one task per boundary for all kv heads, a CTA each
-    const int w = (p.token_major ? (int)blockIdx.x / p.num_kv_heads : (int)blockIdx.x) + 1;
+    const int w = (int)blockIdx.x + 1;
     const int4 task = __ldcg(p.tasks + w);
     // tasks past this call's worker count are stale
     if (w >= plan_workers(W, nw) || task.x < 0) return;
     tok = task.x;
     wf = task.z;
     wl = task.w;
-    kv = p.token_major ? (int)blockIdx.x % p.num_kv_heads : task.y;
+    kv = task.y;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   // The partials: the suffix slots wf .. wl, then (cascade) the prefix chunks.
-  // Worker wf + i's slot: u + wf + i (u = token * Hkv + kv head), or
-  // token-major (token + wf + i) * Hkv + kv head.
+  // Worker wf + i's slot: u + wf + i (u = token * Hkv + kv head).
   const int u = tok * p.num_kv_heads + kv;
   const int ns = wl - wf + 1, n = ns + p.prefix_chunks;
   auto slot = [&](int i) -> const float* {
-    const size_t s0 = p.token_major ? (size_t)(tok + wf + i) * p.num_kv_heads + kv
-                                    : (size_t)(u + wf + i);
+    const size_t s0 = (size_t)(u + wf + i);
     return i < ns ? p.partials + s0 * p.slot_floats
                   : p.prefix_partials +
                         (((size_t)(i - ns) * p.num_tokens + tok) * p.num_kv_heads + kv) *
@@ -236,12 +233,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) pa_merge_tm_kernel(const Mer
 
 template <int D, int G>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
-  // one CTA per slice boundary (and kv head), or per (token, kv head)
-  const int boundaries = p.all_units ? p.num_tokens * p.num_kv_heads
-                                     : (p.num_workers - 1) * (p.token_major ? p.num_kv_heads : 1);
+  // one CTA per slice boundary, or per (token, kv head)
+  const int boundaries = p.all_units ? p.num_tokens * p.num_kv_heads : p.num_workers - 1;
   if (boundaries <= 0) return cudaSuccess;  // one worker: nothing is ever split
+  // token-major partials: eight KV heads, no cascade (the split-KV kernel's own limits)
+  if (p.token_major && (p.all_units || p.prefix_chunks != 0 || p.num_kv_heads > kMergeWarps))
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)boundaries);  // one CTA per slice boundary (and kv head)
+  cfg.gridDim = dim3((unsigned)boundaries);
   cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -252,9 +251,7 @@ cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.token_major && !p.all_units && p.prefix_chunks == 0 &&
-      p.num_kv_heads <= kMergeWarps) {  // a CTA per boundary, a warp per KV head
-    cfg.gridDim = dim3((unsigned)(p.num_workers - 1));
+  if (p.token_major) {  // a CTA per boundary, a warp per KV head
     cfg.blockDim = dim3(32 * p.num_kv_heads);
     return cudaLaunchKernelEx(&cfg, pa_merge_tm_kernel<D, G>, p);
   }
