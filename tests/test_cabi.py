@@ -60,6 +60,10 @@ def test_set_option_validates_values(pa_lib):
         assert pa_lib.pa_set_option(7, v) == -1  # PA_ERR_INVALID_ARG
     assert pa_lib.pa_set_option(7, 1) == 0
     assert pa_lib.pa_set_option(7, 2) == 0
+    # PA_OPT_MIXED_PREFILL_CTAS: 0 (the planner's choice) or a positive share
+    assert pa_lib.pa_set_option(8, -1) == -1
+    assert pa_lib.pa_set_option(8, 12) == 0
+    assert pa_lib.pa_set_option(8, 0) == 0
     assert pa_lib.pa_set_option(99, 1) == -1  # no such option
 
 
