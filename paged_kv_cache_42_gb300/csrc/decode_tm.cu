@@ -15,8 +15,8 @@
 // exchange.
 //
 // Work. The flattened positions are (token, 16-key block): a token's blocks
-// in order, tokens in order; workers (one CTA per SM) take equal contiguous
-// slices. A tile is one position. A token split between workers leaves an
+// in order, tokens in order; workers (one CTA each: two per SM at G <= 4,
+// one at G = 8) take equal contiguous slices. A tile is one position. A token split between workers leaves an
 // fp32 partial per KV head, in slot (token + worker) * 8 + kv head: token +
 // worker grows by one at every token or worker change along the positions,
 // so the slot is unique; the merge pass folds them.
@@ -49,7 +49,7 @@
 // rescales O^T through TMEM first. Sums stay per thread until the token's
 // epilogue (one exchange per token for the heads' sums and maxima).
 //
-// Roles (192 threads, one CTA per SM): warps 0-3 softmax and epilogue, warp 4
+// Roles (192 threads per CTA): warps 0-3 softmax and epilogue, warp 4
 // the producer (walks the work list, one record per tile, two or three tensor
 // copies), warp 5 allocates TMEM and one thread issues the MMAs. Every wait
 // is bounded; one that gives up sets the device error word.
