@@ -16,10 +16,11 @@
 //
 // Work. The flattened positions are (token, 16-key block): a token's blocks
 // in order, tokens in order; workers (one CTA each: two per SM at G <= 4,
-// one at G = 8) take equal contiguous slices. A tile is one position. A token split between workers leaves an
-// fp32 partial per KV head, in slot (token + worker) * 8 + kv head: token +
-// worker grows by one at every token or worker change along the positions,
-// so the slot is unique; the merge pass folds them.
+// one at G = 8) take equal contiguous slices. A tile is one position. A
+// token split between workers leaves an fp32 partial per KV head, in slot
+// (token + worker) * 8 + kv head: token + worker grows by one at every token
+// or worker change along the positions, so the slot is unique; the merge
+// pass folds them.
 //
 // Products (tcgen05.mma kind::f8f6f4 on the cached codes):
 //   S^T = K Q'^T   M = 128 rows (8 KV heads x 16 keys), N = 2 Hq: the token's
