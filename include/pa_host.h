@@ -159,8 +159,9 @@ typedef struct pa_sched_config {
  * newly admitted); request i's tokens are [query_start_loc[i],
  * query_start_loc[i+1]). block_tables is [num_reqs][block_table_stride],
  * the stride being the widest scheduled request's block count (so a step
- * writes no more of the table than it uses), with -1 past each request's
- * blocks; its capacity is max_reqs * max_blocks_per_req entries. */
+ * writes no more of the table than it uses; max_blocks_per_req with
+ * block_tables_retained), with -1 past each request's blocks; its capacity
+ * is max_reqs * max_blocks_per_req entries. */
 typedef struct pa_sched_output {
   int max_reqs, max_tokens, max_preempted; /* capacities */
   int64_t* req_ids;         /* [max_reqs] */
@@ -185,6 +186,16 @@ typedef struct pa_sched_output {
    * requests those whose span starts past it (decode); with their tokens. */
   int num_context_reqs, num_context_tokens;
   int num_generation_reqs, num_generation_tokens;
+  /* Set by the caller. Nonzero selects retained block tables: the row stride
+   * is fixed at the configuration's max_blocks_per_req (so rows stay where
+   * earlier steps put them), and the caller promises that block_tables is
+   * the buffer this scheduler's previous successful step wrote, unmodified
+   * since. The step then writes only what differs from what that step left:
+   * the new blocks of a row whose request and block list carry over (at the
+   * same row), every other row in full. The result is the same table as
+   * writing every row at that stride. A different buffer address than last
+   * time, or a previous step in the other mode, means writing in full. */
+  int block_tables_retained;
 } pa_sched_output;
 
 /* A scheduler drawing blocks from `pool`, which it does not own and which

@@ -31,6 +31,18 @@ struct Req {
   std::vector<Hash> hashes;     // chained hashes of the first full blocks
   int num_registered = 0;       // leading blocks already registered or hit
   bool running = false;
+  // identity of the block list: the request (serial, never reused) and how
+  // often its blocks were released; within one (serial, epoch) the list only
+  // grows at its end
+  uint64_t serial = 0;
+  uint32_t epoch = 0;
+};
+
+// What a block-table row was last written from.
+struct RowSrc {
+  uint64_t serial;
+  uint32_t epoch;
+  int nb;  // blocks written; -1 after them
 };
 
 }  // namespace
@@ -41,6 +53,12 @@ struct pa_scheduler {
   std::unordered_map<int64_t, std::unique_ptr<Req>> reqs;
   std::vector<Req*> running;
   std::deque<Req*> waiting;
+  uint64_t next_serial = 1;
+  // What the last step left in the caller's block table: its address and
+  // stride, and per row the block list it was written from.
+  const int32_t* bt_ptr = nullptr;
+  int bt_stride = 0;
+  std::vector<RowSrc> bt_rows;
 
   int blocks_for(int tokens) const { return (tokens + pool->block_size - 1) / pool->block_size; }
 
@@ -65,6 +83,7 @@ struct pa_scheduler {
     for (auto it = r->blocks.rbegin(); it != r->blocks.rend(); ++it) pool->release(*it);
     r->blocks.clear();
     r->ids.clear();
+    ++r->epoch;
     r->num_registered = 0;
   }
 
@@ -116,6 +135,7 @@ pa_status pa_sched_add_request(pa_scheduler* s, int64_t req_id, const int32_t* p
   try {
     auto r = std::make_unique<Req>();
     r->id = req_id;
+    r->serial = s->next_serial++;
     r->tokens.assign(prompt, prompt + prompt_len);
     r->tokens.reserve(s->cfg.max_model_len);
     r->prompt_len = prompt_len;
@@ -248,6 +268,11 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
   // Emit the batch metadata, then advance the planned state.
   int stride = 1;
   for (auto& e : sched) stride = std::max(stride, (int)e.first->blocks.size());
+  if (out->block_tables_retained) stride = c.max_blocks_per_req;  // a fixed row layout
+  const bool keep = out->block_tables_retained && s->bt_ptr == out->block_tables &&
+                    s->bt_stride == stride;
+  const size_t kept_rows = keep ? s->bt_rows.size() : 0;
+  s->bt_rows.resize(sched.size());
   int t = 0, max_q = 0, max_s = 0, decodes = 0;
   int ctx_reqs = 0, ctx_toks = 0, gen_reqs = 0, gen_toks = 0;
   for (size_t k = 0; k < sched.size(); ++k) {
@@ -260,8 +285,16 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
     out->seq_lens[k] = ctx + n;
     int32_t* row = out->block_tables + (size_t)k * stride;
     const int nb = (int)r->ids.size();
-    std::memcpy(row, r->ids.data(), (size_t)nb * sizeof(int32_t));
-    std::memset(row + nb, 0xFF, (size_t)(stride - nb) * sizeof(int32_t));  // -1 past the blocks
+    RowSrc& src = s->bt_rows[k];
+    if (k < kept_rows && src.serial == r->serial && src.epoch == r->epoch && src.nb <= nb) {
+      // the same list, grown at its end: the row holds its first src.nb ids
+      // and -1 after them
+      std::memcpy(row + src.nb, r->ids.data() + src.nb, (size_t)(nb - src.nb) * sizeof(int32_t));
+    } else {
+      std::memcpy(row, r->ids.data(), (size_t)nb * sizeof(int32_t));
+      std::memset(row + nb, 0xFF, (size_t)(stride - nb) * sizeof(int32_t));  // -1 past the blocks
+    }
+    src = RowSrc{r->serial, r->epoch, nb};
     for (int j = 0; j < n; ++j) {
       const int p = ctx + j;
       out->positions[t + j] = p;
@@ -292,6 +325,8 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
   out->num_context_tokens = ctx_toks;
   out->num_generation_reqs = gen_reqs;
   out->num_generation_tokens = gen_toks;
+  s->bt_ptr = out->block_tables;
+  s->bt_stride = stride;
   for (auto& e : sched) {
     e.first->num_computed += e.second;
     if (c.enable_prefix_caching) s->register_full_blocks(e.first);

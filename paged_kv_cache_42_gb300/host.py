@@ -36,7 +36,8 @@ class SchedOutput(ctypes.Structure):
                 ("num_preempted", _c_i), ("max_query_len", _c_i), ("max_seq_len", _c_i),
                 ("block_table_stride", _c_i), ("num_decode_reqs", _c_i),
                 ("num_context_reqs", _c_i), ("num_context_tokens", _c_i),
-                ("num_generation_reqs", _c_i), ("num_generation_tokens", _c_i)]
+                ("num_generation_reqs", _c_i), ("num_generation_tokens", _c_i),
+                ("block_tables_retained", _c_i)]
 
 
 _READY = False
@@ -132,9 +133,17 @@ class BlockPool:
             self._h = L.pa_pool_create(int(num_blocks), block_size, None)
         if not self._h:
             raise ValueError("pa_pool_create rejected its arguments")
+        # one-element lists shared with the schedulers drawing from this pool,
+        # each holding that scheduler's handle until it is destroyed
+        self._sched_cells = []
 
     def close(self) -> None:
         if getattr(self, "_h", None):
+            # A scheduler releases its blocks into the pool when destroyed, so
+            # any still open goes first: finalizers of objects collected
+            # together may run in any order.
+            for cell in self._sched_cells:
+                _destroy_sched(cell)
             lib().pa_pool_destroy(self._h)
             self._h = None
 
@@ -198,22 +207,39 @@ class BlockPool:
         return out[:n // bs].tolist()
 
 
+def _destroy_sched(cell: list) -> None:
+    if cell[0]:
+        h, cell[0] = cell[0], None
+        lib().pa_sched_destroy(h)
+
+
 class Scheduler:
     """pa_sched_*: the token-budget scheduler over a :class:`BlockPool`."""
 
     def __init__(self, pool: BlockPool, *, token_budget: int, max_model_len: int,
                  max_running: int = 0, long_prefill_threshold: int = 0,
                  max_blocks_per_req: int | None = None, prefix_caching: bool = True,
-                 chunked_prefill: bool = True, max_reqs: int = 4096):
+                 chunked_prefill: bool = True, max_reqs: int = 4096,
+                 retained_block_tables: bool = False):
         bs = lib().pa_pool_block_size(pool.handle)
         self.stride = max_blocks_per_req or -(-max_model_len // bs)
         self.cfg = SchedConfig(token_budget, max_running, long_prefill_threshold, max_model_len,
                                self.stride, int(prefix_caching), int(chunked_prefill))
+        self.retained = bool(retained_block_tables)
         self.pool = pool  # keeps the pool alive
-        self._h = lib().pa_sched_create(pool.handle, ctypes.byref(self.cfg))
-        if not self._h:
+        h = lib().pa_sched_create(pool.handle, ctypes.byref(self.cfg))
+        if not h:
             raise ValueError("pa_sched_create rejected its configuration")
+        self._cell = [h]  # shared with the pool, which may destroy it first
+        pool._sched_cells.append(self._cell)
         self._alloc(max_reqs)
+
+    @property
+    def _h(self):
+        h = self._cell[0]
+        if not h:
+            raise RuntimeError("scheduler closed (or its pool was)")
+        return h
 
     def _alloc(self, max_reqs: int) -> None:
         T = self.cfg.token_budget
@@ -228,15 +254,18 @@ class Scheduler:
         a = self._arrays
         o = SchedOutput()
         o.max_reqs, o.max_tokens, o.max_preempted = max_reqs, T, max_reqs
+        # retained tables: the buffer is this object's alone (step() returns
+        # copies), so the scheduler may leave entries as its last step wrote them
+        o.block_tables_retained = int(self.retained)
         for k, v in a.items():
             setattr(o, k, v.ctypes.data_as(_i64p if v.dtype == np.int64 else _i32p))
         self._out = o
         self._max_reqs = max_reqs
 
     def close(self) -> None:
-        if getattr(self, "_h", None):
-            lib().pa_sched_destroy(self._h)
-            self._h = None
+        cell = getattr(self, "_cell", None)  # absent if the constructor raised
+        if cell is not None:
+            _destroy_sched(cell)
 
     __del__ = close
 

@@ -431,6 +431,60 @@ def test_prefix_map_under_colliding_digests(host):
         assert pool.lookup(h) == by_hash.get(h, -1)
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_retained_block_tables_match_full_rows(host, seed):
+    """pa_sched_output.block_tables_retained: a step that writes only what
+    changed since its last step leaves the same table as one that writes
+    every row, through admissions, prefix hits, chunked prefills, growth by
+    a block, preemption (a small pool), finishes and reused request ids."""
+    rng = np.random.default_rng(600 + seed)
+    bs = 16
+    shared = rng.integers(0, 1000, 64).tolist()
+    sides = []
+    for retained in (True, False):
+        pool = host.BlockPool(num_blocks=24, block_size=bs)
+        s = host.Scheduler(pool, token_budget=48, max_model_len=256, long_prefill_threshold=24,
+                           max_reqs=64, retained_block_tables=retained)
+        sides.append((pool, s))
+    ops = np.random.default_rng(700 + seed)
+    live, next_id, preempted = set(), 0, 0
+    for it in range(300):
+        if ops.random() < 0.25 and len(live) < 12:
+            n = int(ops.integers(1, 80))
+            prompt = (shared[:int(ops.integers(0, 64))] + ops.integers(0, 1000, n).tolist())[:200]
+            rid = int(ops.integers(0, 6)) if ops.random() < 0.3 else 100 + next_id
+            if rid in live:
+                rid = 100 + next_id
+            next_id += 1
+            for _, s in sides:
+                s.add_request(rid, prompt)
+            live.add(rid)
+        outs = [s.step() for _, s in sides]
+        a, b = outs
+        for k in a:
+            if k != "block_tables":
+                assert np.array_equal(np.asarray(a[k]), np.asarray(b[k])), (it, k)
+        # retained rows are max_blocks_per_req (16) wide: the full-mode rows,
+        # then -1
+        ta, tb = a["block_tables"], b["block_tables"]
+        assert ta.shape == (tb.shape[0], 16), (it, ta.shape)
+        assert np.array_equal(ta[:, :tb.shape[1]], tb), it
+        assert np.all(ta[:, tb.shape[1]:] == -1), it
+        preempted += len(a["preempted_ids"])
+        for rid in a["req_ids"].tolist():
+            st = sides[0][1].request_state(rid)
+            if st["num_computed"] == st["num_tokens"]:
+                if ops.random() < 0.02 or st["num_tokens"] >= 250:
+                    for _, s in sides:
+                        s.finish(rid)
+                    live.discard(rid)
+                else:
+                    tok = int(ops.integers(0, 1000))
+                    for _, s in sides:
+                        s.append_token(rid, tok)
+    assert next_id > 10 and preempted > 0
+
+
 # ---------------------------------------- invariants and random parity ----
 
 class KVModel:
@@ -597,3 +651,23 @@ class _Mut:
 def test_planted_oracle_mistakes_break_a_pin(mutant, runner):
     with pytest.raises(AssertionError):
         runner(OracleSide(mutant))
+
+
+def test_pool_closed_before_its_scheduler(host):
+    # Finalizers of objects collected together run in any order: closing the
+    # pool first must destroy the scheduler still drawing from it (which
+    # releases its blocks into the pool) rather than leave it to release them
+    # into freed memory later.
+    pool = host.BlockPool(num_blocks=8, block_size=16)
+    s = host.Scheduler(pool, token_budget=16, max_model_len=64)
+    s.add_request(0, list(range(40)))
+    s.step()
+    assert pool.num_free() < 8
+    pool.close()
+    with pytest.raises(RuntimeError):
+        s.step()
+    s.close()  # a no-op now
+    s2 = host.Scheduler(host.BlockPool(num_blocks=8, block_size=16), token_budget=16,
+                        max_model_len=64)
+    s2.close()
+    s2.pool.close()
