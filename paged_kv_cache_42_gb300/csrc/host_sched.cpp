@@ -20,22 +20,28 @@ using pa_host::Hash;
 
 namespace {
 
-struct Req {
+// The fields a step reads for every request come first (the first two
+// cache lines of the 64-byte aligned object); the hashes and extra keys,
+// touched only when a block fills or a request arrives, last.
+struct alignas(64) Req {
   int64_t id = 0;
   std::vector<int32_t> tokens;  // prompt, then sampled tokens
-  int prompt_len = 0;
-  std::vector<uint8_t> extra;   // extra hash keys
-  int num_computed = 0;
   std::vector<int> blocks;      // pool indices, logical block order
   std::vector<int32_t> ids;     // the same blocks' physical ids (block-table rows)
-  std::vector<Hash> hashes;     // chained hashes of the first full blocks
+  int num_computed = 0;
+  int prompt_len = 0;
   int num_registered = 0;       // leading blocks already registered or hit
-  bool running = false;
+  // copies of tokens.back() and ids.back(), which a decode's metadata needs
+  // every step (read here, they cost no access to either array)
+  int32_t last_token = 0, last_id = -1;
   // identity of the block list: the request (serial, never reused) and how
   // often its blocks were released; within one (serial, epoch) the list only
   // grows at its end
-  uint64_t serial = 0;
   uint32_t epoch = 0;
+  uint64_t serial = 0;
+  bool running = false;
+  std::vector<Hash> hashes;     // chained hashes of the first full blocks
+  std::vector<uint8_t> extra;   // extra hash keys
 };
 
 // What a block-table row was last written from.
@@ -77,6 +83,7 @@ struct pa_scheduler {
   void add_block(Req* r, int i) {
     r->blocks.push_back(i);
     r->ids.push_back(pool->id[i]);
+    r->last_id = pool->id[i];
   }
 
   void release_blocks(Req* r) {
@@ -137,6 +144,7 @@ pa_status pa_sched_add_request(pa_scheduler* s, int64_t req_id, const int32_t* p
     r->id = req_id;
     r->serial = s->next_serial++;
     r->tokens.assign(prompt, prompt + prompt_len);
+    r->last_token = prompt[prompt_len - 1];
     r->tokens.reserve(s->cfg.max_model_len);
     r->prompt_len = prompt_len;
     if (extra_len) r->extra.assign(extra, extra + extra_len);
@@ -160,6 +168,7 @@ pa_status pa_sched_append_token(pa_scheduler* s, int64_t req_id, int32_t token) 
       (int)r->tokens.size() >= s->cfg.max_model_len)
     return PA_ERR_INVALID_ARG;
   r->tokens.push_back(token);
+  r->last_token = token;
   return PA_OK;
 }
 
@@ -295,11 +304,17 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
       std::memset(row + nb, 0xFF, (size_t)(stride - nb) * sizeof(int32_t));  // -1 past the blocks
     }
     src = RowSrc{r->serial, r->epoch, nb};
-    for (int j = 0; j < n; ++j) {
-      const int p = ctx + j;
-      out->positions[t + j] = p;
-      out->input_tokens[t + j] = r->tokens[p];
-      out->slot_mapping[t + j] = (int64_t)r->ids[p / bs] * bs + p % bs;
+    if (n == 1 && ctx + 1 == (int)r->tokens.size()) {  // a decode: the newest token
+      out->positions[t] = ctx;
+      out->input_tokens[t] = r->last_token;
+      out->slot_mapping[t] = (int64_t)r->last_id * bs + ctx % bs;  // its block is the last
+    } else {
+      for (int j = 0; j < n; ++j) {
+        const int p = ctx + j;
+        out->positions[t + j] = p;
+        out->input_tokens[t + j] = r->tokens[p];
+        out->slot_mapping[t + j] = (int64_t)r->ids[p / bs] * bs + p % bs;
+      }
     }
     t += n;
     max_q = std::max(max_q, n);
