@@ -193,8 +193,8 @@ typedef struct pa_sched_output {
    * since. The step then writes only what differs from what that step left:
    * the new blocks of a row whose request and block list carry over (at the
    * same row), every other row in full. The result is the same table as
-   * writing every row at that stride. A different buffer address than last
-   * time, or a previous step in the other mode, means writing in full. */
+   * writing every row at that stride. A buffer address or row stride other
+   * than the previous step's means writing every row in full. */
   int block_tables_retained;
 } pa_sched_output;
 

@@ -485,6 +485,51 @@ def test_retained_block_tables_match_full_rows(host, seed):
     assert next_id > 10 and preempted > 0
 
 
+def test_retained_mode_toggled_and_buffer_swapped(host):
+    """Switching block_tables_retained on and off between steps, and moving
+    to a new table buffer, leaves every table equal to a full write: a step
+    only reuses rows written into the same buffer at the same stride."""
+    rng = np.random.default_rng(650)
+    sides = []
+    for _ in range(2):
+        pool = host.BlockPool(num_blocks=32, block_size=16)
+        sides.append(host.Scheduler(pool, token_budget=40, max_model_len=256,
+                                    long_prefill_threshold=20, max_reqs=8))
+    a, b = sides  # a toggles and moves; b writes every row at the widest stride
+    live, nid, swaps, reuse_steps = set(), 0, 0, 0
+    for it in range(400):
+        if rng.random() < 0.2 and len(live) < 10:
+            prompt = rng.integers(0, 500, int(rng.integers(1, 60))).tolist()
+            for s in sides:
+                s.add_request(nid, prompt)
+            live.add(nid)
+            nid += 1
+        a.retained = bool(rng.random() < 0.7)
+        a._out.block_tables_retained = int(a.retained)
+        if rng.random() < 0.05:
+            a._alloc(a._max_reqs + 1)  # new buffers at new addresses
+            a._out.block_tables_retained = int(a.retained)
+            swaps += 1
+        oa, ob = a.step(), b.step()
+        reuse_steps += a.retained
+        ta, tb = oa["block_tables"], ob["block_tables"]
+        w = tb.shape[1]
+        assert ta.shape[0] == tb.shape[0] and ta.shape[1] >= w, it
+        assert np.array_equal(ta[:, :w], tb) and np.all(ta[:, w:] == -1), it
+        for rid in oa["req_ids"].tolist():
+            st = a.request_state(rid)
+            if st["num_computed"] == st["num_tokens"]:
+                if rng.random() < 0.05 or st["num_tokens"] >= 250:
+                    for s in sides:
+                        s.finish(rid)
+                    live.discard(rid)
+                else:
+                    tok = int(rng.integers(0, 500))
+                    for s in sides:
+                        s.append_token(rid, tok)
+    assert swaps > 5 and reuse_steps > 100
+
+
 # ---------------------------------------- invariants and random parity ----
 
 class KVModel:
