@@ -705,19 +705,21 @@ def run_ours(args, rank, world, local, dist):
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0 and not args.quick:
         line["host_scheduler"] = host_scheduler_timing()
+        line["host_scheduler"]["xxh64"] = host_scheduler_timing(hash_algo="xxh64", brief=True)
     return line
 
 
-def host_scheduler_timing(steps: int = 200) -> dict:
+def host_scheduler_timing(steps: int = 200, hash_algo: str = "sha256", brief: bool = False) -> dict:
     """Time the library's host scheduler step (pa_sched_step) forming the
     mixed-batch shape: 512 decoding requests with the mixed workload's
     context lengths plus 3 long prompts prefilled in 512-token chunks under
-    a 2048-token budget, prefix caching on. Only the C call is timed."""
+    a 2048-token budget, prefix caching on (block hash: hash_algo). Only the
+    C call is timed."""
     from paged_kv_cache_42_gb300 import host
 
     ctx, _, _ = wl.config_lengths(MIXED_CONFIG)
     rng = np.random.Generator(np.random.PCG64(7))
-    pool = host.BlockPool(num_blocks=90000, block_size=16)
+    pool = host.BlockPool(num_blocks=90000, block_size=16, hash_algo=hash_algo)
     s = host.Scheduler(pool, token_budget=2048, max_model_len=4096, long_prefill_threshold=512,
                        max_reqs=1024, retained_block_tables=True)
     for i, c in enumerate(ctx[:512]):
@@ -751,6 +753,10 @@ def host_scheduler_timing(steps: int = 200) -> dict:
         shapes.add((len(out["req_ids"]), out["num_tokens"]))
         after(out)
     t = np.asarray(times) * 1e6
+    if brief:
+        return {"us_per_step_median": round(float(np.median(t)), 1),
+                "us_per_step_p90": round(float(np.percentile(t, 90)), 1),
+                "what": "the same, with XXH64 block hashes (PA_HASH_XXH64)"}
     return {"us_per_step_median": round(float(np.median(t)), 1),
             "us_per_step_p90": round(float(np.percentile(t, 90)), 1), "steps": steps,
             "batch": "512 decodes + 3 prefill chunks of 512, 2048 tokens",

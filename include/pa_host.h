@@ -23,7 +23,13 @@
  *        || block token ids (int32, little endian) || extra key bytes
  *     (adapter id, multimodal hashes, cache salt; the caller serialises
  *     them, tagged by source). The chaining and SHA-256 come from the pages;
- *     the byte serialisation is this library's own.
+ *     the byte serialisation is this library's own. A pool may select
+ *     instead the faster, non-cryptographic XXH64 over the same bytes (the
+ *     pages' "xxhash variant a flag away"; "Automatic Prefix Caching" on the
+ *     selectable hash algorithm): its 64-bit value, little endian, fills the
+ *     first 8 bytes of the 32-byte hash and the rest are zero. Distinct
+ *     prefixes then collide with probability about n^2 / 2^65 over n cached
+ *     blocks, the trade-off the pages attach to a fast hash.
  *  3. A token-budget scheduler step ("Deep Dive - vLLM", "The V1 scheduler:
  *     one token budget"; "vLLM v1 Deep Dive: How LLM(...) and the Server Boot
  *     and Generate", Part 3 "Step 3 - Scheduler iteration"; "vLLM: An
@@ -111,6 +117,18 @@ int pa_pool_is_cached(const pa_block_pool* pool, int32_t id);
  * (which may exceed max). */
 int pa_pool_free_queue(const pa_block_pool* pool, int32_t* out, int max);
 
+/* Block hash algorithms (pa_pool_set_hash_algo, pa_block_hash_algo). */
+#define PA_HASH_SHA256 0 /* default */
+#define PA_HASH_XXH64 1
+
+/* Select the pool's block hash algorithm: the one the scheduler drawing from
+ * it and pa_pool_find_cached_prefix use. Allowed only while no block holds a
+ * hash (digests of two algorithms never share a table); PA_ERR_INVALID_ARG
+ * otherwise or for an unknown algorithm. */
+pa_status pa_pool_set_hash_algo(pa_block_pool* pool, int algo);
+/* The pool's algorithm, or -1 for a NULL pool. */
+int pa_pool_hash_algo(const pa_block_pool* pool);
+
 /* ---------------------------------------------------------------- hash -- */
 
 /* Chained block hash of tokens[0..num_tokens) (see above) into out.
@@ -119,8 +137,16 @@ int pa_pool_free_queue(const pa_block_pool* pool, int32_t* out, int max);
 void pa_block_hash(const uint8_t parent[32], const int32_t* tokens, int num_tokens,
                    const uint8_t* extra, int extra_len, uint8_t out[32]);
 
+/* The same with the given algorithm (PA_HASH_*); PA_ERR_INVALID_ARG for an
+ * unknown one, out untouched. */
+pa_status pa_block_hash_algo(int algo, const uint8_t parent[32], const int32_t* tokens,
+                             int num_tokens, const uint8_t* extra, int extra_len,
+                             uint8_t out[32]);
+
 /* Plain SHA-256 of len bytes (FIPS 180-4). */
 void pa_sha256(const uint8_t* data, size_t len, uint8_t out[32]);
+/* Plain XXH64 of len bytes with the given seed. */
+uint64_t pa_xxh64(const uint8_t* data, size_t len, uint64_t seed);
 
 /* The longest run of the prompt's full blocks registered in the pool,
  * chained from the first block and stopping at the first miss, limited to

@@ -5,7 +5,8 @@ TEST INFRASTRUCTURE ONLY: the tests (and nothing in the product) use this
 module to check the library's C++ host runtime. It shares no code with it:
 it is written from the pages' description with Python containers (a deque
 for the free queue, dicts for reference counts and the hash map, lists for
-the request queues) and ``hashlib`` for SHA-256, with no attention to speed.
+the request queues), ``hashlib`` for SHA-256 and a plain restatement of
+XXH64 for the fast-hash option, with no attention to speed.
 
 Sources (page title, section):
   * "Deep Dive - vLLM", "Block pool, prefix cache, and eviction": reference
@@ -44,22 +45,77 @@ from collections import deque
 
 ZERO_HASH = bytes(32)
 
+_M64 = (1 << 64) - 1
+# XXH64's five constants, as its published description gives them
+_XP = (0x9E3779B185EBCA87, 0xC2B2AE3D27D4EB4F, 0x165667B19E3779F9, 0x85EBCA77C2B2AE63,
+       0x27D4EB2F165667C5)
 
-def block_hash(parent: bytes | None, tokens, extra: bytes = b"") -> bytes:
+
+def _rotl64(x: int, r: int) -> int:
+    return ((x << r) | (x >> (64 - r))) & _M64
+
+
+def _xround(acc: int, lane: int) -> int:
+    return _rotl64((acc + lane * _XP[1]) & _M64, 31) * _XP[0] & _M64
+
+
+def xxh64(data: bytes, seed: int = 0) -> int:
+    """XXH64 of ``data`` (the xxHash family's 64-bit function, by its
+    published description): four accumulators over 32-byte stripes, folded
+    and merged; then the length, 8-byte words, a 4-byte word and single
+    bytes mixed in; then the final avalanche. Words are little endian."""
+    data = bytes(data)
+    n, pos = len(data), 0
+    word = lambda at, size: int.from_bytes(data[at:at + size], "little")
+    if n >= 32:
+        acc = [(seed + _XP[0] + _XP[1]) & _M64, (seed + _XP[1]) & _M64, seed & _M64,
+               (seed - _XP[0]) & _M64]
+        while n - pos >= 32:
+            acc = [_xround(acc[k], word(pos + 8 * k, 8)) for k in range(4)]
+            pos += 32
+        h = sum(_rotl64(a, r) for a, r in zip(acc, (1, 7, 12, 18))) & _M64
+        for a in acc:
+            h = ((h ^ _xround(0, a)) * _XP[0] + _XP[3]) & _M64
+    else:
+        h = (seed + _XP[4]) & _M64
+    h = (h + n) & _M64
+    while n - pos >= 8:
+        h = (_rotl64(h ^ _xround(0, word(pos, 8)), 27) * _XP[0] + _XP[3]) & _M64
+        pos += 8
+    if n - pos >= 4:
+        h = (_rotl64(h ^ (word(pos, 4) * _XP[0] & _M64), 23) * _XP[1] + _XP[2]) & _M64
+        pos += 4
+    for b in data[pos:]:
+        h = _rotl64(h ^ (b * _XP[4] & _M64), 11) * _XP[0] & _M64
+    for shift, mul in ((33, _XP[1]), (29, _XP[2]), (32, None)):
+        h ^= h >> shift
+        if mul is not None:
+            h = h * mul & _M64
+    return h
+
+
+def block_hash(parent: bytes | None, tokens, extra: bytes = b"", algo: str = "sha256") -> bytes:
     """Chained hash of one block ("Deep Dive - vLLM", "Block pool, prefix
     cache, and eviction": hash of the parent hash, the block tokens and the
-    extra keys; SHA-256 by default)."""
+    extra keys; SHA-256 by default, a faster xxhash variant selectable).
+    ``algo`` "xxh64": the 64-bit XXH64 of the same bytes, little endian, in
+    the first 8 of 32 bytes."""
     data = (parent if parent is not None else ZERO_HASH) + struct.pack(
         "<%di" % len(tokens), *[int(t) for t in tokens]) + bytes(extra)
+    if algo == "xxh64":
+        return xxh64(data).to_bytes(8, "little") + bytes(24)
+    if algo != "sha256":
+        raise ValueError(f"unknown hash algorithm {algo!r}")
     return hashlib.sha256(data).digest()
 
 
-def prompt_block_hashes(tokens, block_size: int, extra: bytes = b"") -> list:
+def prompt_block_hashes(tokens, block_size: int, extra: bytes = b"",
+                        algo: str = "sha256") -> list:
     """Hashes of every full block of ``tokens``, each chained to the one
     before it."""
     out, parent = [], None
     for b in range(len(tokens) // block_size):
-        parent = block_hash(parent, tokens[b * block_size:(b + 1) * block_size], extra)
+        parent = block_hash(parent, tokens[b * block_size:(b + 1) * block_size], extra, algo)
         out.append(parent)
     return out
 
@@ -80,11 +136,14 @@ class Pool:
     """Block pool: reference counts, an LRU free queue and the prefix-cache
     map ("Deep Dive - vLLM", "Block pool, prefix cache, and eviction")."""
 
-    def __init__(self, ids, block_size: int):
+    def __init__(self, ids, block_size: int, hash_algo: str = "sha256"):
         ids = [int(i) for i in ids]
         if len(set(ids)) != len(ids) or any(i < 0 for i in ids) or block_size <= 0:
             raise ValueError("ids must be distinct and >= 0; block_size > 0")
+        if hash_algo not in ("sha256", "xxh64"):
+            raise ValueError(f"unknown hash algorithm {hash_algo!r}")
         self.block_size = block_size
+        self.hash_algo = hash_algo
         self.refs = {i: 0 for i in ids}
         self.hash_of = {}       # block id -> hash
         self.block_of = {}      # hash -> block id
@@ -150,7 +209,8 @@ class Pool:
         first miss, within num_tokens - 1 tokens."""
         limit = (len(tokens) - 1) // self.block_size
         hits = []
-        for h in prompt_block_hashes(tokens[:limit * self.block_size], self.block_size, extra):
+        for h in prompt_block_hashes(tokens[:limit * self.block_size], self.block_size, extra,
+                                     self.hash_algo):
             slot = self.block_of.get(h)
             if slot is None:
                 break
@@ -316,7 +376,8 @@ class Scheduler:
             old = r.num_computed
             r.num_computed += n
             if self.prefix_caching:
-                hashes = prompt_block_hashes(r.tokens[:r.num_computed // bs * bs], bs, r.extra)
+                hashes = prompt_block_hashes(r.tokens[:r.num_computed // bs * bs], bs, r.extra,
+                                             pool.hash_algo)
                 for b in range(old // bs, r.num_computed // bs):
                     if r.blocks[b] not in pool.hash_of:
                         pool.cache_block(r.blocks[b], hashes[b])

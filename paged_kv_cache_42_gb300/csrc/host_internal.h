@@ -38,9 +38,14 @@ class Sha256 {
   uint64_t total_ = 0;
 };
 
-// Chained block hash: SHA-256(parent || tokens as int32 LE || extra).
-Hash block_hash(const Hash* parent, const int32_t* tokens, int n, const uint8_t* extra,
-                int extra_len);
+// XXH64 of n bytes (host_xxh64.cpp).
+uint64_t xxh64(const uint8_t* p, size_t n, uint64_t seed);
+
+// Chained block hash over parent || tokens as int32 LE || extra: SHA-256
+// (PA_HASH_SHA256), or XXH64 in the first 8 bytes, little endian, and zeros
+// after them (PA_HASH_XXH64).
+Hash block_hash(int algo, const Hash* parent, const int32_t* tokens, int n,
+                const uint8_t* extra, int extra_len);
 
 }  // namespace pa_host
 
@@ -65,6 +70,7 @@ struct pa_block_pool {
   std::vector<Slot> table;
   size_t mask = 0;
   int head = -1, tail = -1, num_free = 0;
+  int hash_algo = PA_HASH_SHA256;  // of every digest in the table
 
   int find(int32_t pid) const {
     auto it = index.find(pid);

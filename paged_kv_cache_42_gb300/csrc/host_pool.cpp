@@ -185,6 +185,16 @@ int32_t pa_pool_lookup(const pa_block_pool* pool, const uint8_t hash[32]) {
   return i < 0 ? -1 : pool->id[i];
 }
 
+pa_status pa_pool_set_hash_algo(pa_block_pool* pool, int algo) {
+  if (!pool || (algo != PA_HASH_SHA256 && algo != PA_HASH_XXH64)) return PA_ERR_INVALID_ARG;
+  for (uint8_t h : pool->has_hash)
+    if (h) return PA_ERR_INVALID_ARG;  // digests of one algorithm per table
+  pool->hash_algo = algo;
+  return PA_OK;
+}
+
+int pa_pool_hash_algo(const pa_block_pool* pool) { return pool ? pool->hash_algo : -1; }
+
 int pa_pool_ref_count(const pa_block_pool* pool, int32_t id) {
   const int i = pool ? pool->find(id) : -1;
   return i < 0 ? -1 : pool->ref[i];
@@ -215,8 +225,8 @@ int pa_pool_find_cached_prefix(const pa_block_pool* pool, const int32_t* tokens,
   Hash parent;
   int hits = 0;
   for (int b = 0; b < limit; ++b) {
-    parent = pa_host::block_hash(b ? &parent : nullptr, tokens + (size_t)b * bs, bs, extra,
-                                 extra_len);
+    parent = pa_host::block_hash(pool->hash_algo, b ? &parent : nullptr, tokens + (size_t)b * bs,
+                                 bs, extra, extra_len);
     const int i = pool->lookup(parent);
     if (i < 0) break;  // a chained hash cannot match past a miss
     out_ids[hits++] = pool->id[i];

@@ -41,6 +41,7 @@ struct alignas(64) Req {
   uint64_t serial = 0;
   bool running = false;
   std::vector<Hash> hashes;     // chained hashes of the first full blocks
+  int hashes_algo = PA_HASH_SHA256;  // the algorithm they were taken with
   std::vector<uint8_t> extra;   // extra hash keys
 };
 
@@ -69,12 +70,17 @@ struct pa_scheduler {
   int blocks_for(int tokens) const { return (tokens + pool->block_size - 1) / pool->block_size; }
 
   // Chained hashes of the request's first n full blocks (tokens only grow,
-  // so hashes once computed stay valid, across preemption too).
+  // so hashes once computed stay valid, across preemption too - unless the
+  // pool's algorithm changed, which it can only while no block holds one).
   void ensure_hashes(Req* r, int n) {
     const int bs = pool->block_size;
+    if (r->hashes_algo != pool->hash_algo) {
+      r->hashes.clear();
+      r->hashes_algo = pool->hash_algo;
+    }
     while ((int)r->hashes.size() < n) {
       const int b = (int)r->hashes.size();
-      r->hashes.push_back(pa_host::block_hash(b ? &r->hashes[b - 1] : nullptr,
+      r->hashes.push_back(pa_host::block_hash(pool->hash_algo, b ? &r->hashes[b - 1] : nullptr,
                                               r->tokens.data() + (size_t)b * bs, bs,
                                               r->extra.data(), (int)r->extra.size()));
     }

@@ -11,6 +11,7 @@
 // derived here from that definition with exact integer roots rather than
 // typed in: floor(frac(root(p)) * 2^32) = floor(root(p * 2^(32k))) mod 2^32.
 #include <algorithm>
+#include <vector>
 
 #include "host_internal.h"
 
@@ -122,11 +123,37 @@ void Sha256::final(uint8_t out[32]) {
   }
 }
 
-Hash block_hash(const Hash* parent, const int32_t* tokens, int n, const uint8_t* extra,
-                int extra_len) {
-  Sha256 s;
+Hash block_hash(int algo, const Hash* parent, const int32_t* tokens, int n,
+                const uint8_t* extra, int extra_len) {
   static const Hash zero{};
-  s.update((parent ? *parent : zero).data(), 32);
+  const uint8_t* const par = (parent ? *parent : zero).data();
+  if (extra_len <= 0) extra = nullptr;
+  if (algo == PA_HASH_XXH64) {
+    // one contiguous copy of the same bytes, then a single pass
+    const size_t len = 32 + (size_t)4 * n + (extra ? (size_t)extra_len : 0);
+    uint8_t small[32 + 4 * 64 + 64];
+    std::vector<uint8_t> big;
+    uint8_t* buf = small;
+    if (len > sizeof small) {
+      big.resize(len);
+      buf = big.data();
+    }
+    std::memcpy(buf, par, 32);
+    for (int i = 0; i < n; ++i) {
+      const uint32_t v = (uint32_t)tokens[i];
+      buf[32 + 4 * i] = (uint8_t)v;
+      buf[33 + 4 * i] = (uint8_t)(v >> 8);
+      buf[34 + 4 * i] = (uint8_t)(v >> 16);
+      buf[35 + 4 * i] = (uint8_t)(v >> 24);
+    }
+    if (extra) std::memcpy(buf + 32 + (size_t)4 * n, extra, (size_t)extra_len);
+    const uint64_t h = xxh64(buf, len, 0);
+    Hash out{};
+    for (int i = 0; i < 8; ++i) out[i] = (uint8_t)(h >> (8 * i));
+    return out;
+  }
+  Sha256 s;
+  s.update(par, 32);
   uint8_t le[256];  // tokens as int32 little endian, in chunks of 64
   for (int i0 = 0; i0 < n; i0 += 64) {
     const int m = std::min(64, n - i0);
@@ -139,7 +166,7 @@ Hash block_hash(const Hash* parent, const int32_t* tokens, int n, const uint8_t*
     }
     s.update(le, (size_t)4 * m);
   }
-  if (extra && extra_len > 0) s.update(extra, (size_t)extra_len);
+  if (extra) s.update(extra, (size_t)extra_len);
   Hash out;
   s.final(out.data());
   return out;
@@ -153,11 +180,19 @@ extern "C" void pa_sha256(const uint8_t* data, size_t len, uint8_t out[32]) {
   s.final(out);
 }
 
-extern "C" void pa_block_hash(const uint8_t parent[32], const int32_t* tokens, int num_tokens,
-                              const uint8_t* extra, int extra_len, uint8_t out[32]) {
+extern "C" pa_status pa_block_hash_algo(int algo, const uint8_t parent[32],
+                                        const int32_t* tokens, int num_tokens,
+                                        const uint8_t* extra, int extra_len, uint8_t out[32]) {
+  if (algo != PA_HASH_SHA256 && algo != PA_HASH_XXH64) return PA_ERR_INVALID_ARG;
   pa_host::Hash p;
   if (parent) std::memcpy(p.data(), parent, 32);
-  const pa_host::Hash h = pa_host::block_hash(parent ? &p : nullptr, tokens,
+  const pa_host::Hash h = pa_host::block_hash(algo, parent ? &p : nullptr, tokens,
                                               num_tokens > 0 ? num_tokens : 0, extra, extra_len);
   std::memcpy(out, h.data(), 32);
+  return PA_OK;
+}
+
+extern "C" void pa_block_hash(const uint8_t parent[32], const int32_t* tokens, int num_tokens,
+                              const uint8_t* extra, int extra_len, uint8_t out[32]) {
+  pa_block_hash_algo(PA_HASH_SHA256, parent, tokens, num_tokens, extra, extra_len, out);
 }

@@ -67,6 +67,11 @@ def lib() -> ctypes.CDLL:
         L.pa_block_hash.restype = None
         L.pa_sha256.argtypes = [_u8p, ctypes.c_size_t, ctypes.c_char_p]
         L.pa_sha256.restype = None
+        L.pa_block_hash_algo.argtypes = [_c_i, _u8p, _i32p, _c_i, _u8p, _c_i, ctypes.c_char_p]
+        L.pa_xxh64.argtypes = [_u8p, ctypes.c_size_t, ctypes.c_uint64]
+        L.pa_xxh64.restype = ctypes.c_uint64
+        L.pa_pool_set_hash_algo.argtypes = [_c_p, _c_i]
+        L.pa_pool_hash_algo.argtypes = [_c_p]
         L.pa_pool_find_cached_prefix.argtypes = [_c_p, _i32p, _c_i, _u8p, _c_i, _i32p, _c_i]
         L.pa_reusable_tokens.argtypes = [_c_i, _c_i, _c_i, ctypes.POINTER(_c_i)]
         L.pa_sched_create.argtypes = [_c_p, ctypes.POINTER(SchedConfig)]
@@ -105,10 +110,18 @@ def sha256(data: bytes) -> bytes:
     return out.raw
 
 
-def block_hash(parent: bytes | None, tokens, extra: bytes = b"") -> bytes:
+HASH_ALGOS = {"sha256": 0, "xxh64": 1}  # PA_HASH_SHA256, PA_HASH_XXH64
+
+
+def xxh64(data: bytes, seed: int = 0) -> int:
+    return int(lib().pa_xxh64(bytes(data), len(data), seed))
+
+
+def block_hash(parent: bytes | None, tokens, extra: bytes = b"", algo: str = "sha256") -> bytes:
     t = _i32(tokens)
     out = ctypes.create_string_buffer(32)
-    lib().pa_block_hash(parent, _p32(t), int(t.size), bytes(extra) or None, len(extra), out)
+    _check(lib().pa_block_hash_algo(HASH_ALGOS[algo], parent, _p32(t), int(t.size),
+                                    bytes(extra) or None, len(extra), out), "pa_block_hash_algo")
     return out.raw
 
 
@@ -123,7 +136,8 @@ class BlockPool:
     """pa_pool_*: physical blocks with reference counts, the free queue and
     the prefix-cache map."""
 
-    def __init__(self, num_blocks: int | None = None, block_size: int = 16, ids=None):
+    def __init__(self, num_blocks: int | None = None, block_size: int = 16, ids=None,
+                 hash_algo: str = "sha256"):
         L = lib()
         if ids is not None:
             arr = _i32(ids)
@@ -133,6 +147,11 @@ class BlockPool:
             self._h = L.pa_pool_create(int(num_blocks), block_size, None)
         if not self._h:
             raise ValueError("pa_pool_create rejected its arguments")
+        if hash_algo not in HASH_ALGOS:
+            L.pa_pool_destroy(self._h)
+            self._h = None
+            raise ValueError(f"unknown hash algorithm {hash_algo!r}")
+        _check(L.pa_pool_set_hash_algo(self._h, HASH_ALGOS[hash_algo]), "pa_pool_set_hash_algo")
         # one-element lists shared with the schedulers drawing from this pool,
         # each holding that scheduler's handle until it is destroyed
         self._sched_cells = []
@@ -152,6 +171,15 @@ class BlockPool:
     @property
     def handle(self):
         return self._h
+
+    @property
+    def hash_algo(self) -> str:
+        v = lib().pa_pool_hash_algo(self._h)
+        return next(k for k, a in HASH_ALGOS.items() if a == v)
+
+    def set_hash_algo(self, algo: str) -> None:
+        """Only while no block holds a hash."""
+        _check(lib().pa_pool_set_hash_algo(self._h, HASH_ALGOS[algo]), "pa_pool_set_hash_algo")
 
     def num_free(self) -> int:
         return lib().pa_pool_num_free(self._h)

@@ -327,6 +327,86 @@ def test_block_hash_chain(host):
     assert host.block_hash(None, t, b"lora:a") != host.block_hash(None, t, b"salt:a")
 
 
+# ------------------------------------------------------------------ XXH64 --
+
+XXH64_GOLD = json.load(open(os.path.join(HERE, "golden", "xxh64_vectors.json")))["vectors"]
+
+
+@pytest.mark.parametrize("v", XXH64_GOLD, ids=lambda v: repr(v["input"][:12]))
+def test_xxh64_published_values(host, v):
+    want = int(v["digest"], 16)
+    assert host_ref.xxh64(v["input"].encode(), v["seed"]) == want
+    assert host.xxh64(v["input"].encode(), v["seed"]) == want
+
+
+def test_xxh64_library_and_oracle_agree_at_every_length(host):
+    # the published values reach the 32-byte stripes, the 4-byte word and
+    # the byte tail; lengths 0..300 also reach every count of 8-byte words
+    rng = np.random.default_rng(17)
+    for n in range(301):
+        data = rng.integers(0, 256, n, dtype=np.uint8).tobytes()
+        seed = int(rng.integers(0, 2**63)) if n % 3 else 0
+        assert host.xxh64(data, seed) == host_ref.xxh64(data, seed), n
+
+
+def test_xxh64_planted_mistakes_break_a_published_value(monkeypatch):
+    # a wrong constant or a dropped final step in the oracle's XXH64 fails
+    # one of the published values
+    def fails():
+        return any(host_ref.xxh64(v["input"].encode(), v["seed"]) != int(v["digest"], 16)
+                   for v in XXH64_GOLD)
+    for k in range(5):
+        bad = list(host_ref._XP)
+        bad[k] ^= 1 << 40
+        monkeypatch.setattr(host_ref, "_XP", tuple(bad))
+        assert fails(), k
+        monkeypatch.undo()
+    monkeypatch.setattr(host_ref, "_rotl64", lambda x, r: ((x << (r + 1)) | (x >> (63 - r))) & host_ref._M64)
+    assert fails()
+
+
+def test_block_hash_chain_xxh64(host):
+    rng = np.random.default_rng(5)
+    parent = None
+    for _ in range(6):
+        t = rng.integers(-2**31, 2**31 - 1, 16, dtype=np.int64).astype(np.int32)
+        extra = rng.integers(0, 256, rng.integers(0, 300), dtype=np.uint8).tobytes()
+        got = host.block_hash(parent, t, extra, algo="xxh64")
+        assert got == host_ref.block_hash(parent, t.tolist(), extra, algo="xxh64")
+        assert got[8:] == bytes(24)
+        parent = got
+    # chaining: the parent changes the digest
+    t = list(range(16))
+    assert host.block_hash(None, t, algo="xxh64") != host.block_hash(b"\x01" * 32, t, algo="xxh64")
+
+
+def test_pool_hash_algo_switches_only_while_empty(host):
+    p = host.BlockPool(num_blocks=4, block_size=16)
+    assert p.hash_algo == "sha256"
+    p.set_hash_algo("xxh64")
+    assert p.hash_algo == "xxh64"
+    b = p.allocate(1)[0]
+    p.cache_block(b, b"\x07" * 32)
+    with pytest.raises(RuntimeError):
+        p.set_hash_algo("sha256")  # a digest is in the table
+    with pytest.raises(ValueError):
+        host.BlockPool(num_blocks=4, block_size=16, hash_algo="md5")
+    # a scheduler over an xxh64 pool finds its own prefix again
+    pool = host.BlockPool(num_blocks=16, block_size=4, hash_algo="xxh64")
+    s = host.Scheduler(pool, token_budget=64, max_model_len=64)
+    prompt = list(range(20))
+    s.add_request(0, prompt)
+    s.step()
+    s.finish(0)
+    want = [host.block_hash(None, prompt[:4], algo="xxh64")]
+    for k in range(1, 4):
+        want.append(host.block_hash(want[-1], prompt[4 * k:4 * k + 4], algo="xxh64"))
+    assert [pool.lookup(h) >= 0 for h in want] == [True] * 4
+    s.add_request(1, prompt)
+    out = s.step()
+    assert out["num_computed"][0] == 16  # four cached blocks, the fifth recomputed
+
+
 # ------------------------------------------------------------ host errors --
 
 def test_pool_rejects_bad_calls(host):
@@ -562,7 +642,7 @@ def check_invariants(sched, pool, out, budget, bs, kv: KVModel):
             assert kv.slot.get(r.blocks[p // bs] * bs + p % bs) == r.tokens[p], (r.id, p)
 
 
-def random_run(seed: int, lib_host=None, steps: int = 120):
+def random_run(seed: int, lib_host=None, steps: int = 120, algo: str = "sha256"):
     rng = np.random.default_rng(seed)
     bs = int(rng.choice([2, 4, 16]))
     n_blocks = int(rng.integers(6, 40))
@@ -573,10 +653,10 @@ def random_run(seed: int, lib_host=None, steps: int = 120):
                long_prefill_threshold=int(rng.choice([0, 0, 3, 7])),
                prefix_caching=bool(rng.integers(0, 4)), chunked_prefill=bool(rng.integers(0, 4)))
     ids = rng.permutation(1000)[:n_blocks].tolist()
-    o_pool = host_ref.Pool(ids, bs)
+    o_pool = host_ref.Pool(ids, bs, hash_algo=algo)
     o = host_ref.Scheduler(o_pool, **cfg)
     if lib_host is not None:
-        l_pool = lib_host.BlockPool(ids=ids, block_size=bs)
+        l_pool = lib_host.BlockPool(ids=ids, block_size=bs, hash_algo=algo)
         lib = lib_host.Scheduler(l_pool, **cfg)
     kv = KVModel()
     prefixes = [rng.integers(0, 5, int(rng.integers(1, 3 * bs))).tolist() for _ in range(3)]
@@ -612,6 +692,10 @@ def random_run(seed: int, lib_host=None, steps: int = 120):
                       "num_generation_tokens"):
                 assert got[k] == out[k], (seed, step, k)
             assert l_pool.free_queue() == list(o_pool.free), (seed, step)
+            # the same digests, under the same blocks
+            for h, b in o_pool.block_of.items():
+                assert l_pool.lookup(h) == b, (seed, step)
+            assert sum(l_pool.is_cached(b) for b in ids) == len(o_pool.block_of), (seed, step)
         for rid in list(out["req_ids"]):
             r = o.reqs[rid]
             if r.num_computed == len(r.tokens):
@@ -628,18 +712,20 @@ def random_run(seed: int, lib_host=None, steps: int = 120):
     return n_preempt, n_hits
 
 
-def test_oracle_invariants_random():
+@pytest.mark.parametrize("algo", ["sha256", "xxh64"])
+def test_oracle_invariants_random(algo):
     total_pre = total_hits = 0
     for seed in range(30):
-        p, h = random_run(seed)
+        p, h = random_run(seed, algo=algo)
         total_pre += p
         total_hits += h
     assert total_pre > 0 and total_hits > 0  # the sweep reaches preemption and prefix hits
 
 
-def test_library_matches_oracle_random(host):
+@pytest.mark.parametrize("algo", ["sha256", "xxh64"])
+def test_library_matches_oracle_random(host, algo):
     for seed in range(100, 160):
-        random_run(seed, lib_host=host)
+        random_run(seed, lib_host=host, algo=algo)
 
 
 # ----------------------------------------------- planted oracle mistakes --
