@@ -56,6 +56,7 @@ struct pa_block_pool {
   std::unordered_map<int32_t, int> index;
   std::vector<int> ref, prev, next;
   std::vector<uint8_t> in_free, has_hash;
+  std::vector<int> uses;  // all zero between calls: pa_pool_free's per-block count
   std::vector<pa_host::Hash> hash;
   // The prefix cache's hash -> block map: open addressing with linear probing
   // over a power-of-two table at least twice the block count (so a probe

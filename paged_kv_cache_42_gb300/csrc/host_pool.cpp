@@ -112,6 +112,7 @@ pa_block_pool* pa_pool_create(int num_blocks, int block_size, const int32_t* ids
     p->next.assign(num_blocks, -1);
     p->in_free.assign(num_blocks, 0);
     p->has_hash.assign(num_blocks, 0);
+    p->uses.assign(num_blocks, 0);
     p->hash.resize(num_blocks);
     size_t slots = 2;
     while (slots < 2 * (size_t)num_blocks) slots *= 2;
@@ -149,13 +150,26 @@ pa_status pa_pool_allocate(pa_block_pool* pool, int n, int32_t* out_ids) {
 
 pa_status pa_pool_free(pa_block_pool* pool, const int32_t* ids, int n) {
   if (!pool || n < 0 || (n > 0 && !ids)) return PA_ERR_INVALID_ARG;
-  // Validate everything first (an id may repeat): nothing changes on error.
-  std::unordered_map<int, int> uses;
-  for (int k = 0; k < n; ++k) {
+  // Validate everything first (an id may repeat, at most as often as the
+  // block is referenced): nothing changes on error. The counts live in a
+  // zeroed per-pool array and are put back to zero before returning.
+  int k = 0;
+  bool ok = true;
+  for (; k < n; ++k) {
     const int i = pool->find(ids[k]);
-    if (i < 0 || ++uses[i] > pool->ref[i]) return PA_ERR_INVALID_ARG;
+    if (i < 0) {
+      ok = false;
+      break;
+    }
+    if (++pool->uses[i] > pool->ref[i]) {
+      ++k;  // this one was counted
+      ok = false;
+      break;
+    }
   }
-  for (int k = n - 1; k >= 0; --k) pool->release(pool->find(ids[k]));
+  for (int j = 0; j < k; ++j) pool->uses[pool->find(ids[j])] = 0;
+  if (!ok) return PA_ERR_INVALID_ARG;
+  for (int j = n - 1; j >= 0; --j) pool->release(pool->find(ids[j]));
   return PA_OK;
 }
 

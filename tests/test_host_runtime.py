@@ -430,6 +430,21 @@ def test_pool_rejects_bad_calls(host):
     assert p.lookup(b"\1" * 32) == ids[0] and not p.is_cached(ids[1])
 
 
+def test_rejected_release_changes_nothing(host):
+    # a release naming a block more often than it is referenced, or an
+    # unknown id, is refused whole; the next valid release then succeeds
+    p = host.BlockPool(num_blocks=6, block_size=16)
+    a = p.allocate(3)
+    p.touch([a[0]])  # two references
+    queue = p.free_queue()
+    for bad in ([a[0], a[0], a[0]], [a[1], 99], [a[2], a[2]], [77], [a[0], a[1], a[1]]):
+        with pytest.raises(RuntimeError):
+            p.release(bad)
+        assert [p.ref_count(b) for b in a] == [2, 1, 1] and p.free_queue() == queue
+    p.release([a[0], a[0], a[1]])
+    assert [p.ref_count(b) for b in a] == [0, 0, 1] and p.num_free() == 5
+
+
 def test_scheduler_rejects_bad_calls(host):
     p = host.BlockPool(num_blocks=8, block_size=16)
     with pytest.raises(ValueError):
