@@ -50,9 +50,12 @@
  *        (planned state, before the GPU runs) and its newly full blocks are
  *        registered in the prefix cache.
  *
- * All functions are host-only and synchronous; none touches the GPU. Memory
- * is allocated only inside the create/add calls. Objects are not
- * thread-safe. Negative return values are pa_status codes.
+ * All functions are host-only and synchronous; none touches the GPU. The
+ * pool allocates only in pa_pool_create. The scheduler allocates in its
+ * create and add calls, and a step may grow storage it keeps (a request's
+ * block and hash lists, its queues and per-step lists; amortised, reused
+ * from step to step). Hashing and lookups allocate nothing. Objects are
+ * not thread-safe. Negative return values are pa_status codes.
  */
 #ifndef PA_HOST_H
 #define PA_HOST_H

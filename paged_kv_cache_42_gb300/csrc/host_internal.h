@@ -38,7 +38,21 @@ class Sha256 {
   uint64_t total_ = 0;
 };
 
-// XXH64 of n bytes (host_xxh64.cpp).
+// XXH64 (host_xxh64.cpp), streaming: whole 32-byte stripes go through the
+// four accumulators as they arrive, a partial one is carried.
+class Xxh64 {
+ public:
+  explicit Xxh64(uint64_t seed);
+  void update(const uint8_t* data, size_t len);
+  uint64_t digest() const;
+
+ private:
+  uint64_t v_[4];
+  uint8_t buf_[32];
+  size_t buf_len_ = 0;
+  uint64_t total_ = 0;
+  uint64_t seed_;
+};
 uint64_t xxh64(const uint8_t* p, size_t n, uint64_t seed);
 
 // Chained block hash over parent || tokens as int32 LE || extra: SHA-256

@@ -66,6 +66,10 @@ struct pa_scheduler {
   const int32_t* bt_ptr = nullptr;
   int bt_stride = 0;
   std::vector<RowSrc> bt_rows;
+  // a step's scheduled list and one admission's prefix hits, kept between
+  // steps so that their storage is reused
+  std::vector<std::pair<Req*, int>> sched;
+  std::vector<int> hits;
 
   int blocks_for(int tokens) const { return (tokens + pool->block_size - 1) / pool->block_size; }
 
@@ -210,7 +214,8 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
     return PA_ERR_INVALID_ARG;
 
   int budget = c.token_budget;
-  std::vector<std::pair<Req*, int>> sched;
+  std::vector<std::pair<Req*, int>>& sched = s->sched;
+  sched.clear();
   int num_preempted = 0;
 
   // Pass 1: running requests, in order.
@@ -247,7 +252,8 @@ pa_status pa_sched_step(pa_scheduler* s, pa_sched_output* out) {
   while (num_preempted == 0 && !s->waiting.empty() && budget > 0) {
     if (c.max_running > 0 && (int)s->running.size() >= c.max_running) break;
     Req* r = s->waiting.front();
-    std::vector<int> hits;
+    std::vector<int>& hits = s->hits;
+    hits.clear();
     if (c.enable_prefix_caching) {
       const int max_hit = ((int)r->tokens.size() - 1) / bs;
       s->ensure_hashes(r, max_hit);

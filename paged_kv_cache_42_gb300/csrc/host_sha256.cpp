@@ -11,7 +11,6 @@
 // derived here from that definition with exact integer roots rather than
 // typed in: floor(frac(root(p)) * 2^32) = floor(root(p * 2^(32k))) mod 2^32.
 #include <algorithm>
-#include <vector>
 
 #include "host_internal.h"
 
@@ -129,25 +128,22 @@ Hash block_hash(int algo, const Hash* parent, const int32_t* tokens, int n,
   const uint8_t* const par = (parent ? *parent : zero).data();
   if (extra_len <= 0) extra = nullptr;
   if (algo == PA_HASH_XXH64) {
-    // one contiguous copy of the same bytes, then a single pass
-    const size_t len = 32 + (size_t)4 * n + (extra ? (size_t)extra_len : 0);
-    uint8_t small[32 + 4 * 64 + 64];
-    std::vector<uint8_t> big;
-    uint8_t* buf = small;
-    if (len > sizeof small) {
-      big.resize(len);
-      buf = big.data();
+    Xxh64 x(0);
+    x.update(par, 32);
+    uint8_t le[256];  // tokens as int32 little endian, in chunks of 64
+    for (int i0 = 0; i0 < n; i0 += 64) {
+      const int m = std::min(64, n - i0);
+      for (int i = 0; i < m; ++i) {
+        const uint32_t v = (uint32_t)tokens[i0 + i];
+        le[4 * i] = (uint8_t)v;
+        le[4 * i + 1] = (uint8_t)(v >> 8);
+        le[4 * i + 2] = (uint8_t)(v >> 16);
+        le[4 * i + 3] = (uint8_t)(v >> 24);
+      }
+      x.update(le, (size_t)4 * m);
     }
-    std::memcpy(buf, par, 32);
-    for (int i = 0; i < n; ++i) {
-      const uint32_t v = (uint32_t)tokens[i];
-      buf[32 + 4 * i] = (uint8_t)v;
-      buf[33 + 4 * i] = (uint8_t)(v >> 8);
-      buf[34 + 4 * i] = (uint8_t)(v >> 16);
-      buf[35 + 4 * i] = (uint8_t)(v >> 24);
-    }
-    if (extra) std::memcpy(buf + 32 + (size_t)4 * n, extra, (size_t)extra_len);
-    const uint64_t h = xxh64(buf, len, 0);
+    if (extra) x.update(extra, (size_t)extra_len);
+    const uint64_t h = x.digest();
     Hash out{};
     for (int i = 0; i < 8; ++i) out[i] = (uint8_t)(h >> (8 * i));
     return out;

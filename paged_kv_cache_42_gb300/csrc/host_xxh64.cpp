@@ -12,6 +12,8 @@
 // 8-byte words, one 4-byte word and single bytes are mixed in, and a final
 // avalanche of shifts and multiplies spreads every input bit over the
 // result. Words are read little endian, whatever the host's byte order.
+#include <cstring>
+
 #include "host_internal.h"
 
 namespace pa_host {
@@ -41,26 +43,45 @@ inline uint64_t merge(uint64_t h, uint64_t acc) { return (h ^ round(0, acc)) * P
 
 }  // namespace
 
-uint64_t xxh64(const uint8_t* p, size_t n, uint64_t seed) {
-  const uint8_t* const end = p + n;
-  uint64_t h;
-  if (n >= 32) {
-    uint64_t v1 = seed + P1 + P2, v2 = seed + P2, v3 = seed, v4 = seed - P1;
-    for (; end - p >= 32; p += 32) {
-      v1 = round(v1, le64(p));
-      v2 = round(v2, le64(p + 8));
-      v3 = round(v3, le64(p + 16));
-      v4 = round(v4, le64(p + 24));
-    }
-    h = rotl(v1, 1) + rotl(v2, 7) + rotl(v3, 12) + rotl(v4, 18);
-    h = merge(h, v1);
-    h = merge(h, v2);
-    h = merge(h, v3);
-    h = merge(h, v4);
-  } else {
-    h = seed + P5;
+Xxh64::Xxh64(uint64_t seed) : seed_(seed) {
+  v_[0] = seed + P1 + P2;
+  v_[1] = seed + P2;
+  v_[2] = seed;
+  v_[3] = seed - P1;
+}
+
+void Xxh64::update(const uint8_t* p, size_t n) {
+  total_ += n;
+  if (buf_len_ + n < 32) {  // not a whole stripe yet
+    if (n) std::memcpy(buf_ + buf_len_, p, n);
+    buf_len_ += n;
+    return;
   }
-  h += (uint64_t)n;
+  if (buf_len_) {  // complete the carried stripe
+    const size_t take = 32 - buf_len_;
+    std::memcpy(buf_ + buf_len_, p, take);
+    for (int k = 0; k < 4; ++k) v_[k] = round(v_[k], le64(buf_ + 8 * k));
+    p += take;
+    n -= take;
+    buf_len_ = 0;
+  }
+  for (; n >= 32; p += 32, n -= 32)
+    for (int k = 0; k < 4; ++k) v_[k] = round(v_[k], le64(p + 8 * k));
+  if (n) std::memcpy(buf_, p, n);
+  buf_len_ = n;
+}
+
+uint64_t Xxh64::digest() const {
+  uint64_t h;
+  if (total_ >= 32) {
+    h = rotl(v_[0], 1) + rotl(v_[1], 7) + rotl(v_[2], 12) + rotl(v_[3], 18);
+    for (int k = 0; k < 4; ++k) h = merge(h, v_[k]);
+  } else {
+    h = seed_ + P5;
+  }
+  h += total_;
+  const uint8_t* p = buf_;
+  const uint8_t* const end = buf_ + buf_len_;
   for (; end - p >= 8; p += 8) h = rotl(h ^ round(0, le64(p)), 27) * P1 + P4;
   if (end - p >= 4) {
     h = rotl(h ^ (uint64_t)le32(p) * P1, 23) * P2 + P3;
@@ -73,6 +94,12 @@ uint64_t xxh64(const uint8_t* p, size_t n, uint64_t seed) {
   h *= P3;
   h ^= h >> 32;
   return h;
+}
+
+uint64_t xxh64(const uint8_t* p, size_t n, uint64_t seed) {
+  Xxh64 x(seed);
+  x.update(p, n);
+  return x.digest();
 }
 
 }  // namespace pa_host
